@@ -1,0 +1,203 @@
+"""Seeded synthetic workloads for DSA sparse attention with IndexShare.
+
+This module only draws random tensors of the right shapes and distributions.
+It holds none of the method's arithmetic (no scores, no selection, no
+attention), so both the CUDA path and the CPU oracle can take their inputs
+from it without sharing any computation.
+
+Shapes and distributions follow the five decode / prefill / MTP workloads of
+the GLM-5.2 DSA + IndexShare description (GLM-5.2 config: ``index_topk=2048``,
+``index_topk_freq=4``, ``kv_lora_rank=512``, 64 attention heads, maximum
+position 1048576):
+
+* indexer queries ``q_idx`` [B, Q, 64, 128] and keys ``k_idx`` [B, T, 128]:
+  N(0, 1)/sqrt(128), rounded to bf16.  3% of the cached positions of every
+  sequence (exactly ``round(0.03*T)``, drawn without replacement) get ``2*u``
+  added to their key, ``u`` being one random unit vector shared by the whole
+  workload.  The per-coordinate std is sigma = 1/sqrt(128), so ``2*u`` is a
+  displacement of 2*sigma*sqrt(128): twice the typical key norm.  Adding
+  2*sigma*u literally would move q.k by a small fraction of its spread and
+  would not make the top-k selection structured.
+* head weights ``w`` [B, Q, 64]: U(0, 1)/64, fp32.
+* MLA queries ``q`` [B, Q, 64, 576] and latent cache ``kv`` [B, T, 576] per
+  layer: N(0, 1), bf16 (512 latent dims then 64 already-rotated RoPE dims).
+* query positions ``q_pos`` [B, Q] int32.
+
+Every tensor has its own seed, derived from (workload seed, tensor, layer,
+step).  Values depend on the device's generator: a tensor drawn on the GPU is
+not the one drawn on the CPU with the same seed, so parity checks always copy
+one drawn tensor to both sides.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+N_IDX_HEADS = 64
+IDX_DIM = 128
+N_HEADS = 64
+KV_LORA_RANK = 512
+ROPE_DIM = 64
+D_QK = KV_LORA_RANK + ROPE_DIM  # 576
+D_V = KV_LORA_RANK              # 512
+TOPK = 2048
+TOPK_FREQ = 4                   # layers per IndexShare group
+MTP_STEPS = 7
+SM_SCALE = 1.0 / math.sqrt(D_QK)
+BOOST_FRACTION = 0.03
+BOOST_SCALE = 2.0
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic workload.
+
+    ``kind`` is "decode" (one IndexShare group over Q query tokens per
+    sequence), "prefill" (a chunk of Q new tokens at the end of the context)
+    or "mtp" (one indexer pass at the last position, then ``mtp_steps`` draft
+    attentions that reuse its indices).
+    """
+    name: str
+    kind: str
+    B: int
+    Q: int
+    T: int
+    first_pos: int          # q_pos[b, q] = first_pos + q
+    n_layers: int = TOPK_FREQ
+    mtp_steps: int = 0
+    topk: int = TOPK
+    seed: int = 0
+
+    def q_positions(self) -> torch.Tensor:
+        pos = torch.arange(self.first_pos, self.first_pos + self.Q, dtype=torch.int32)
+        return pos.unsqueeze(0).expand(self.B, self.Q).contiguous()
+
+    @property
+    def rows(self) -> int:
+        return self.B * self.Q
+
+    def describe(self) -> dict:
+        d = dataclasses.asdict(self)
+        d["boost_fraction"] = BOOST_FRACTION
+        return d
+
+
+# The five workloads: tiny decode, 128K decode, 1M decode, chunked prefill, MTP.
+TINY = Workload("tiny_decode_T8192", "decode", B=1, Q=4, T=8192, first_pos=8188, seed=100)
+DECODE_128K = Workload("decode_B32_T131072", "decode", B=32, Q=1, T=131072, first_pos=131071, seed=200)
+DECODE_1M = Workload("decode_B8_T1048576", "decode", B=8, Q=1, T=1048576, first_pos=1048575, seed=300)
+PREFILL = Workload("prefill_Q4096_T131072", "prefill", B=1, Q=4096, T=131072, first_pos=126976, seed=400)
+MTP = Workload("mtp_B64_T262144_S7", "mtp", B=64, Q=1, T=262144, first_pos=262143,
+               n_layers=1, mtp_steps=MTP_STEPS, seed=500)
+
+WORKLOADS = {w.name: w for w in (TINY, DECODE_128K, DECODE_1M, PREFILL, MTP)}
+
+_TENSOR_IDS = {"q_idx": 1, "k_idx": 2, "w": 3, "q": 4, "kv": 5, "boost_pos": 6, "boost_dir": 7, "q_step": 8}
+
+
+def tensor_seed(base: int, tensor: str, layer: int = 0, step: int = 0) -> int:
+    """Seed of one tensor: a fixed mix of the workload seed and the tensor's role."""
+    return (base * 1_000_003 + _TENSOR_IDS[tensor] * 10_007 + layer * 101 + step * 7) & 0x7FFF_FFFF
+
+
+def _gen(device, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def indexer_keys(B: int, T: int, seed: int, device="cpu", boost: bool = True) -> torch.Tensor:
+    """k_idx [B, T, 128] bf16: N(0,1)/sqrt(128) with 3% of positions shifted by 2u."""
+    k = torch.randn(B, T, IDX_DIM, generator=_gen(device, tensor_seed(seed, "k_idx")),
+                    device=device, dtype=torch.float32)
+    k.mul_(1.0 / math.sqrt(IDX_DIM))
+    if boost and T > 0:
+        u = torch.randn(IDX_DIM, generator=_gen(device, tensor_seed(seed, "boost_dir")),
+                        device=device, dtype=torch.float32)
+        u = u / u.norm()
+        n_boost = int(round(BOOST_FRACTION * T))
+        gp = _gen(device, tensor_seed(seed, "boost_pos"))
+        for b in range(B):
+            pos = torch.randperm(T, generator=gp, device=device)[:n_boost]
+            k[b, pos] += BOOST_SCALE * u
+    return k.to(torch.bfloat16)
+
+
+def indexer_queries(B: int, Q: int, seed: int, device="cpu") -> torch.Tensor:
+    """q_idx [B, Q, 64, 128] bf16: N(0,1)/sqrt(128)."""
+    q = torch.randn(B, Q, N_IDX_HEADS, IDX_DIM, generator=_gen(device, tensor_seed(seed, "q_idx")),
+                    device=device, dtype=torch.float32)
+    return (q * (1.0 / math.sqrt(IDX_DIM))).to(torch.bfloat16)
+
+
+def head_weights(B: int, Q: int, seed: int, device="cpu") -> torch.Tensor:
+    """w [B, Q, 64] fp32: U(0,1)/64."""
+    w = torch.rand(B, Q, N_IDX_HEADS, generator=_gen(device, tensor_seed(seed, "w")),
+                   device=device, dtype=torch.float32)
+    return w / N_IDX_HEADS
+
+
+def mla_queries(B: int, Q: int, seed: int, layer: int = 0, device="cpu") -> torch.Tensor:
+    """q [B, Q, 64, 576] bf16: N(0,1)."""
+    return torch.randn(B, Q, N_HEADS, D_QK, generator=_gen(device, tensor_seed(seed, "q", layer)),
+                       device=device, dtype=torch.bfloat16)
+
+
+def latent_cache(B: int, T: int, seed: int, layer: int = 0, device="cpu") -> torch.Tensor:
+    """kv [B, T, 576] bf16: N(0,1) (512 latent dims, then 64 rotated RoPE dims)."""
+    return torch.randn(B, T, D_QK, generator=_gen(device, tensor_seed(seed, "kv", layer)),
+                       device=device, dtype=torch.bfloat16)
+
+
+def draft_queries(S: int, B: int, seed: int, device="cpu") -> torch.Tensor:
+    """q_steps [S, B, 64, 576] bf16: an independent N(0,1) query per draft step."""
+    out = torch.empty(S, B, N_HEADS, D_QK, device=device, dtype=torch.bfloat16)
+    for s in range(S):
+        out[s] = torch.randn(B, N_HEADS, D_QK, generator=_gen(device, tensor_seed(seed, "q_step", 0, s + 1)),
+                             device=device, dtype=torch.bfloat16)
+    return out
+
+
+@dataclasses.dataclass
+class Inputs:
+    q_idx: torch.Tensor
+    w: torch.Tensor
+    k_idx: torch.Tensor
+    q_pos: torch.Tensor
+    q: list            # per layer [B, Q, 64, 576]   (decode / prefill)
+    kv: list           # per layer [B, T, 576]
+    q_steps: Optional[torch.Tensor] = None   # [S, B, 64, 576] (mtp)
+    idx_q: Optional[list] = None             # per-layer indexer queries (per-layer variant)
+    idx_w: Optional[list] = None
+    idx_k: Optional[list] = None
+
+
+def make_inputs(wl: Workload, device="cpu", per_layer_indexers: bool = False,
+                B: Optional[int] = None, T: Optional[int] = None) -> Inputs:
+    """Draw every tensor of a workload (optionally with a smaller B or T)."""
+    B = wl.B if B is None else B
+    T = wl.T if T is None else T
+    first = wl.first_pos if T == wl.T else T - (wl.T - wl.first_pos)
+    pos = torch.arange(first, first + wl.Q, dtype=torch.int32)
+    q_pos = pos.unsqueeze(0).expand(B, wl.Q).contiguous().to(device)
+    q_idx = indexer_queries(B, wl.Q, wl.seed, device)
+    w = head_weights(B, wl.Q, wl.seed, device)
+    k_idx = indexer_keys(B, T, wl.seed, device)
+    qs, kvs = [], []
+    for layer in range(wl.n_layers):
+        if wl.kind != "mtp":
+            qs.append(mla_queries(B, wl.Q, wl.seed, layer, device))
+        kvs.append(latent_cache(B, T, wl.seed, layer, device))
+    q_steps = draft_queries(wl.mtp_steps, B, wl.seed, device) if wl.kind == "mtp" else None
+    inp = Inputs(q_idx, w, k_idx, q_pos, qs, kvs, q_steps)
+    if per_layer_indexers:
+        inp.idx_q, inp.idx_w, inp.idx_k = [q_idx], [w], [k_idx]
+        for layer in range(1, wl.n_layers):
+            s = wl.seed + 17 * layer
+            inp.idx_q.append(indexer_queries(B, wl.Q, s, device))
+            inp.idx_w.append(head_weights(B, wl.Q, s, device))
+            inp.idx_k.append(indexer_keys(B, T, s, device))
+    return inp
