@@ -1,0 +1,542 @@
+#!/usr/bin/env python
+"""Benchmark: one IndexShare group step of DSA sparse attention on B300.
+
+A step is one pass of the whole hot path over one batch: the indexer scores
+every cached position, the top-2048 are selected, and 4 sparse MLA layers
+attend over them (MTP drafting: one indexer pass + 7 draft steps).  The
+default workload is decode over a 1M-token context (B = 8 sequences, one
+query token each).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Prints one JSON line on rank 0.  Under torchrun every rank runs its own batch
+(weak scaling, no collective on the data path); the step time is the max over
+ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from long_context_sparse_26_b300 import workloads as wl  # noqa: E402
+
+METRIC = "4-layer IndexShare group decode tokens/s @1M ctx; % of HBM roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = wl.DECODE_1M.name
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
+
+
+# --------------------------------------------------------------------------- helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1400.0, "fallback"
+
+
+def algorithmic_bytes(w: wl.Workload, B: int) -> dict:
+    """Indexer keys read once per group + gathered latent rows (576 bf16) per layer or draft step."""
+    key_bytes = B * w.T * wl.IDX_DIM * 2
+    uses = w.mtp_steps if w.kind == "mtp" else w.n_layers
+    gather = uses * B * w.Q * w.topk * wl.D_QK * 2
+    return {"indexer_keys": key_bytes, "gathered_rows": gather, "total": key_bytes + gather}
+
+
+def indexer_flops(w: wl.Workload, B: int) -> int:
+    """Multiply-adds x2 of the indexer over the causal (query, key) pairs."""
+    pos = np.arange(w.first_pos, w.first_pos + w.Q)
+    pairs = int(np.minimum(pos + 1, w.T).sum()) * B
+    return 2 * wl.N_IDX_HEADS * wl.IDX_DIM * pairs
+
+
+class ClockSampler:
+    """Polls NVML (read-only) for the SM clock and clock-event reasons."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
+
+    def __init__(self, device_index: int, period_s: float = 0.01):
+        self.samples = []
+        self.period = period_s
+        self._stop = threading.Event()
+        self._mark = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception:  # NVML unavailable: no clock record
+            self.nv = None
+            self.max_mhz = None
+        self.t = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+                reasons = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append((time.perf_counter(), mhz, reasons))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def start(self):
+        if self.nv is not None:
+            self.t.start()
+        return self
+
+    def stop(self):
+        self._stop.set()
+        if self.nv is not None:
+            self.t.join()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if self.nv is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1] or self.samples
+        mhz = [s[1] for s in inside]
+        bits = 0
+        for s in inside:
+            bits |= s[2]
+        reasons = [name for bit, name in self.REASONS.items() if bits & bit]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside)}
+
+
+def count_graph_kernels(graph) -> int | None:
+    """Kernel nodes in a captured CUDA graph (every kernel in it is libdsa's)."""
+    try:
+        from cuda.bindings import runtime as rt
+        g = rt.cudaGraph_t(init_value=graph.raw_cuda_graph())
+        err, _, n = rt.cudaGraphGetNodes(g, 0)
+        err, nodes, n = rt.cudaGraphGetNodes(g, n)
+        if err != rt.cudaError_t.cudaSuccess:
+            return None
+        count = 0
+        for node in nodes[:n]:
+            err, ty = rt.cudaGraphNodeGetType(node)
+            if ty == rt.cudaGraphNodeType.cudaGraphNodeTypeKernel:
+                count += 1
+        return count
+    except Exception:
+        return None
+
+
+def kernel_source_hash(name: str) -> str:
+    with open(os.path.join(ROOT, "long_context_sparse_26_b300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:12]
+
+
+def profiled_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 4 and parts[0] == kernel_file and parts[1] == workload:
+                    if parts[2] == kernel_source_hash(kernel_file):
+                        return float(parts[3])
+    except OSError:
+        pass
+    return None
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- CPU oracle sample
+
+class LazyRows:
+    """Indexable view of one sequence's device latent cache: kv[positions] is
+    copied to the host as fp64 only for the positions asked for."""
+
+    def __init__(self, kv_seq: torch.Tensor):
+        self.kv = kv_seq
+
+    def __getitem__(self, pos):
+        import oracle
+        rows = self.kv[torch.as_tensor(np.asarray(pos), device=self.kv.device)].cpu()
+        return oracle.bf16_bits_to_f64(rows.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def oracle_sample(w: wl.Workload, inp: wl.Inputs, b: int, t: int) -> float:
+    """Times the oracle on one query token of sequence b: the full indexer row,
+    the stable sort, and every attention layer (or draft step).  Returns seconds."""
+    import oracle
+    bits = lambda x: x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    qi, kk = bits(inp.q_idx[b, t]), bits(inp.k_idx[b])
+    wv = inp.w[b, t].detach().cpu().double().numpy()
+    pos = int(inp.q_pos[b, t])
+    if w.kind == "mtp":
+        qs = [bits(inp.q_steps[s, b]) for s in range(w.mtp_steps)]
+        kvs = [LazyRows(inp.kv[0][b])] * w.mtp_steps
+    else:
+        qs = [bits(q[b, t]) for q in inp.q]
+        kvs = [LazyRows(kv[b]) for kv in inp.kv]
+    t0 = time.perf_counter()
+    S = oracle.indexer_scores_row(oracle.bf16_bits_to_f64(qi), wv, oracle.bf16_bits_to_f64(kk), pos)
+    idx = oracle.topk_select_row(S, pos, w.topk)
+    for q, kv in zip(qs, kvs):
+        oracle.sparse_mla_attn_row(oracle.bf16_bits_to_f64(q), kv, idx, wl.SM_SCALE)
+    return time.perf_counter() - t0
+
+
+def cpu_info() -> dict:
+    cores = len(os.sched_getaffinity(0))
+    blas = None
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        blas = max((i.get("num_threads", 0) for i in info), default=None)
+    except Exception:
+        pass
+    return {"cores": blas or cores, "host_cores": cores}
+
+
+def cpu_baseline(w: wl.Workload, inp: wl.Inputs, budget_s: float = 20.0) -> dict:
+    """The oracle, as it stands, on a bounded sample of the workload: query tokens
+    one at a time until about `budget_s` seconds of CPU work."""
+    B, Q = inp.q_idx.shape[0], inp.q_idx.shape[1]
+    rows = [(b, t) for t in range(Q) for b in range(B)]
+    rng = np.random.default_rng(0)
+    if len(rows) > 1:
+        rows = [rows[i] for i in rng.permutation(len(rows))]
+    spent, n = 0.0, 0
+    for (b, t) in rows:
+        spent += oracle_sample(w, inp, b, t)
+        n += 1
+        if spent >= budget_s:
+            break
+    info = cpu_info()
+    uses = w.mtp_steps if w.kind == "mtp" else w.n_layers
+    what = "draft steps" if w.kind == "mtp" else "layers"
+    return {"value": n / spent, "unit": UNIT, "cores": info["cores"], "host_cores": info["host_cores"],
+            "kind": "oracle", "seconds": spent,
+            "sample": f"{n} of {B * Q} query tokens of {w.name}, each: fp64 indexer over its causal keys, "
+                      f"full stable sort, {uses} {what} of exact-softmax attention over its top-{w.topk}"}
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | None:
+    from long_context_sparse_26_b300 import binding as dsa
+    from long_context_sparse_26_b300.build import build_library
+    if rank == 0 or not os.path.exists(os.path.join(ROOT, "long_context_sparse_26_b300", "libdsa.so")):
+        build_library()
+    barrier(world)
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    cfg = dsa.default_config(topk=w.topk)
+    inp = wl.make_inputs(w, dev)
+    B, Q, T = w.B, w.Q, w.T
+    stream = torch.cuda.Stream(device=dev)
+    n_att = w.mtp_steps if w.kind == "mtp" else w.n_layers
+    ws = dsa.alloc_workspace(cfg, B, Q, T, n_att, dev)
+    scores = torch.empty(B, Q, T, device=dev)
+    idx = torch.empty(B, Q, w.topk, dtype=torch.int32, device=dev)
+    if w.kind == "mtp":
+        out = torch.empty(w.mtp_steps, B, 64, 512, dtype=torch.bfloat16, device=dev)
+        outs = [out]
+
+        def step():
+            dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, stream)
+            dsa.topk_select(cfg, scores, inp.q_pos, idx, ws, stream)
+            dsa.mtp_draft_attn(cfg, idx, inp.q_steps, inp.kv[0], out, ws, stream)
+    else:
+        outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(w.n_layers)]
+
+        def step():
+            dsa.indexshare_group_forward(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, inp.q, inp.kv, outs, idx,
+                                         ws, stream)
+
+    torch.cuda.synchronize()
+    # capture one step in a CUDA graph (launch overhead off the critical path)
+    with torch.cuda.stream(stream):
+        step()   # attributes and tensor-map encoders initialised outside capture
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph(keep_graph=True)
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    launches_per_step = count_graph_kernels(graph)
+    status = dsa.get_device_error(stream)
+    if status != 0:
+        raise RuntimeError(f"device error before timing: {dsa.status_string(status)}")
+
+    clocks = ClockSampler(local).start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(args.steps):
+            graph.replay()
+            ev[i + 1].record(stream)
+    stream.synchronize()
+    t_wall1 = time.perf_counter()
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    total_ms = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    status = dsa.get_device_error(stream)
+    if status != 0:
+        raise RuntimeError(f"device error during timing: {dsa.status_string(status)}")
+
+    # ---- the dominant kernel alone: indexer scores, timed with events on its stream
+    kst = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(kst):
+        for _ in range(3):
+            dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, kst)
+    kst.synchronize()
+    kev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    n_k = max(5, min(50, args.steps))
+    kev[0].record(kst)
+    for _ in range(n_k):
+        dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, kst)
+    kev[1].record(kst)
+    kst.synchronize()
+    clocks.stop()
+    idx_ms = kev[0].elapsed_time(kev[1]) / n_k
+
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = measured_peaks()
+    alg = algorithmic_bytes(w, B)
+    flops = indexer_flops(w, B)
+    tokens = B * Q * world if w.kind != "mtp" else B * w.mtp_steps * world
+    value = tokens / (ms_per_step / 1e3)
+    idx_gbs = alg["indexer_keys"] / (idx_ms / 1e3) / 1e9
+    idx_tfs = flops / (idx_ms / 1e3) / 1e12
+    if w.kind == "prefill":
+        roof = {"bound": "tensor", "achieved": idx_tfs, "peak": bf16_tf, "unit": "TFLOP/s", "frac": idx_tfs / bf16_tf,
+                "traffic": profiled_traffic("indexer.cuh", w.name), "kernel": "indexer_scores_kernel<4>",
+                "kernel_ms": idx_ms, "algorithmic_flops": flops, "peak_source": f"{peak_src} bf16 burst"}
+    else:
+        roof = {"bound": "hbm", "achieved": idx_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": idx_gbs / hbm_gbs,
+                "traffic": profiled_traffic("indexer.cuh", w.name), "kernel": "indexer_scores_kernel<1>",
+                "kernel_ms": idx_ms, "algorithmic_bytes": alg["indexer_keys"], "peak_source": f"{peak_src} hbm copy"}
+    step_gbs = alg["total"] / (ms_per_step / 1e3) / 1e9
+    step_roof = {"algorithmic_bytes": alg["total"], "achieved_gbs": step_gbs, "frac_of_measured_hbm": step_gbs / hbm_gbs,
+                 "frac_of_nominal_8tbs": step_gbs / 8000.0, "roofline_ms": alg["total"] / (hbm_gbs * 1e9) * 1e3}
+    if w.kind == "prefill":
+        t_flops = flops / (bf16_tf * 1e12) * 1e3
+        step_roof["roofline_ms"] = max(step_roof["roofline_ms"], t_flops)
+        step_roof["frac_of_roofline_time"] = step_roof["roofline_ms"] / ms_per_step
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(args, w, cfg, inp, outs, idx, scores, ws, stream, dsa)
+
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "Q": Q, "T": T, "topk": w.topk,
+                   "layers_per_group": w.n_layers if w.kind != "mtp" else 1,
+                   "mtp_steps": w.mtp_steps or None, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (no flush needed)", "graph": "one step captured, replayed"},
+        "roofline": roof, "step_roofline": step_roof,
+        "e2e": e2e,
+        "gpu_launches": (launches_per_step or 0) * args.steps,
+        "gpu_launches_per_step": launches_per_step,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "step_ms_median": statistics.median(step_ms),
+    }
+    if w.name == wl.DECODE_1M.name and not args.no_variant:
+        res["per_layer_indexer"] = run_per_layer_variant(args, w, cfg, inp, dev, ms_per_step, dsa)
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_budget)
+    return res
+
+
+def run_e2e(args, w, cfg, inp, outs, idx, scores, ws, stream, dsa) -> dict:
+    """Per step: pinned host -> device copy of the step's new inputs (query-side
+    tensors; the indexer key cache and latent caches stay resident in HBM as
+    the model's state), the step through the C ABI, device -> host copy of the
+    outputs.  Timed with events on the stream."""
+    if w.kind == "mtp":
+        dev_in = [inp.q_idx, inp.w, inp.q_pos, inp.q_steps]
+    else:
+        dev_in = [inp.q_idx, inp.w, inp.q_pos] + list(inp.q)
+    host_in = [t.detach().cpu().pin_memory() for t in dev_in]
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def one():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        if w.kind == "mtp":
+            dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, stream)
+            dsa.topk_select(cfg, scores, inp.q_pos, idx, ws, stream)
+            dsa.mtp_draft_attn(cfg, idx, inp.q_steps, inp.kv[0], outs[0], ws, stream)
+        else:
+            dsa.indexshare_group_forward(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, inp.q, inp.kv, outs, idx,
+                                         ws, stream)
+        for h, o in zip(host_out, outs):
+            h.copy_(o, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            one()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            one()
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    tokens = w.B * w.Q if w.kind != "mtp" else w.B * w.mtp_steps
+    return {"value": tokens / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "api": "long_context_sparse_26_b300.binding (C ABI via ctypes)"}
+
+
+def run_per_layer_variant(args, w, cfg, inp, dev, group_ms, dsa) -> dict:
+    """Without IndexShare: each of the 4 layers runs its own indexer + top-k."""
+    per = wl.make_inputs(w, dev, per_layer_indexers=True)
+    B, Q, T = w.B, w.Q, w.T
+    stream = torch.cuda.Stream(device=dev)
+    ws = dsa.alloc_workspace(cfg, B, Q, T, 1, dev)
+    scores = torch.empty(B, Q, T, device=dev)
+    idxs = [torch.empty(B, Q, w.topk, dtype=torch.int32, device=dev) for _ in range(w.n_layers)]
+    outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(w.n_layers)]
+
+    def step():
+        for layer in range(w.n_layers):
+            dsa.indexer_scores(cfg, per.idx_q[layer], per.idx_w[layer], per.idx_k[layer], per.q_pos, scores, stream)
+            dsa.topk_select(cfg, scores, per.q_pos, idxs[layer], ws, stream)
+            dsa.sparse_mla_attn(cfg, inp.q[layer], inp.kv[layer], idxs[layer], outs[layer], None, ws, stream)
+
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    alg = w.n_layers * B * T * wl.IDX_DIM * 2 + w.n_layers * B * Q * w.topk * wl.D_QK * 2
+    del per
+    torch.cuda.empty_cache()
+    return {"ms_per_step": ms, "tokens_per_s": B * Q / (ms / 1e3), "algorithmic_bytes": alg,
+            "indexshare_speedup": ms / group_ms,
+            "predicted_speedup_bytes": alg / algorithmic_bytes(w, B)["total"]}
+
+
+# --------------------------------------------------------------------------- reference arm (CPU oracle)
+
+def run_reference(args, w: wl.Workload) -> dict:
+    """The oracle as it stands on the host cores; each step = one query token of the workload."""
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = wl.make_inputs(w, dev, B=1)
+    times = []
+    for i in range(args.warmup + args.steps):
+        s = oracle_sample(w, inp, 0, i % w.Q)
+        if i >= args.warmup:
+            times.append(s)
+    per_tok = statistics.mean(times)
+    tokens_per_step = w.mtp_steps if w.kind == "mtp" else 1
+    value = tokens_per_step / per_tok
+    info = cpu_info()
+    uses = w.mtp_steps if w.kind == "mtp" else w.n_layers
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_tok * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Q": w.Q, "T": w.T, "topk": w.topk, "sample_B": 1},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": info["cores"], "host_cores": info["host_cores"],
+                         "kind": "oracle",
+                         "sample": f"each step: one query token of {w.name} (fp64 indexer, full stable sort, "
+                                   f"{uses} attention {'steps' if w.kind == 'mtp' else 'layers'})"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variant", action="store_true", help="skip the per-layer-indexer comparison")
+    ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = wl.WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return
+    res = run_ours(args, w, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+"""Thin ctypes binding of libdsa (include/dsa.h), with the same names.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  Tensors are torch CUDA tensors (device memory and streams come from
+PyTorch); each call enqueues on the current torch stream unless a stream is
+given.  If libdsa.so is missing, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa.so")
+
+STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_ALIGNMENT",
+          4: "DSA_ERR_WORKSPACE", 5: "DSA_ERR_CUDA", 6: "DSA_ERR_DEVICE_CHECK", 7: "DSA_ERR_TIMEOUT"}
+
+# every symbol include/dsa.h declares
+EXPORTS = ("dsa_config_default", "dsa_workspace_bytes", "dsa_indexer_scores", "dsa_topk_select",
+           "dsa_sparse_mla_attn", "dsa_indexshare_group_forward", "dsa_mtp_draft_attn",
+           "dsa_status_string", "dsa_get_device_error")
+
+
+class DsaConfig(ctypes.Structure):
+    _fields_ = [("n_idx_heads", ctypes.c_int), ("idx_dim", ctypes.c_int), ("topk", ctypes.c_int),
+                ("topk_freq", ctypes.c_int), ("kv_lora_rank", ctypes.c_int), ("rope_dim", ctypes.c_int),
+                ("n_heads", ctypes.c_int), ("sm_scale", ctypes.c_float), ("index_share_for_mtp", ctypes.c_int)]
+
+
+class DsaError(RuntimeError):
+    def __init__(self, what: str, status: int):
+        super().__init__(f"{what} failed: {STATUS.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+_VP, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_CFG = ctypes.POINTER(DsaConfig)
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libdsa.so (built in-tree by long_context_sparse_26_b300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m long_context_sparse_26_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        L.dsa_config_default.argtypes = [_CFG]
+        L.dsa_config_default.restype = None
+        L.dsa_workspace_bytes.argtypes = [_CFG, _I, _I, _I, _I]
+        L.dsa_workspace_bytes.restype = _SZ
+        L.dsa_indexer_scores.argtypes = [_CFG, _VP, _VP, _VP, _VP, _I, _I, _I, _VP, _VP]
+        L.dsa_topk_select.argtypes = [_CFG, _VP, _VP, _I, _I, _I, _VP, _VP, _SZ, _VP]
+        L.dsa_sparse_mla_attn.argtypes = [_CFG, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP, _SZ, _VP]
+        L.dsa_indexshare_group_forward.argtypes = [_CFG, _VP, _VP, _VP, _VP, ctypes.POINTER(_VP),
+                                                   ctypes.POINTER(_VP), _I, _I, _I, _I, ctypes.POINTER(_VP),
+                                                   _VP, _VP, _SZ, _VP]
+        L.dsa_mtp_draft_attn.argtypes = [_CFG, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _SZ, _VP]
+        for name in ("dsa_indexer_scores", "dsa_topk_select", "dsa_sparse_mla_attn",
+                     "dsa_indexshare_group_forward", "dsa_mtp_draft_attn", "dsa_get_device_error"):
+            getattr(L, name).restype = ctypes.c_int
+        L.dsa_get_device_error.argtypes = [_VP]
+        L.dsa_status_string.argtypes = [ctypes.c_int]
+        L.dsa_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def default_config(topk: int = 2048) -> DsaConfig:
+    cfg = DsaConfig()
+    lib().dsa_config_default(ctypes.byref(cfg))
+    cfg.topk = topk
+    return cfg
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype or t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor with {ndim} dims, got {t.dtype} {tuple(t.shape)}")
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise DsaError(what, status)
+
+
+def workspace_bytes(cfg: DsaConfig, B: int, Q: int, T: int, n_layers: int) -> int:
+    return int(lib().dsa_workspace_bytes(ctypes.byref(cfg), B, Q, T, n_layers))
+
+
+def alloc_workspace(cfg: DsaConfig, B: int, Q: int, T: int, n_layers: int, device="cuda") -> torch.Tensor:
+    n = workspace_bytes(cfg, B, Q, T, n_layers)
+    if n == 0:
+        raise DsaError("dsa_workspace_bytes", 1)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def indexer_scores(cfg, q_idx, w, k_idx, q_pos, scores, stream=None):
+    """q_idx [B,Q,64,128] bf16, w [B,Q,64] f32, k_idx [B,T,128] bf16, q_pos [B,Q] i32 -> scores [B,Q,T] f32."""
+    _need(q_idx, "q_idx", torch.bfloat16, 4); _need(w, "w", torch.float32, 3)
+    _need(k_idx, "k_idx", torch.bfloat16, 3); _need(q_pos, "q_pos", torch.int32, 2)
+    _need(scores, "scores", torch.float32, 3)
+    B, Q, T = q_idx.shape[0], q_idx.shape[1], k_idx.shape[1]
+    _check(lib().dsa_indexer_scores(ctypes.byref(cfg), _p(q_idx), _p(w), _p(k_idx), _p(q_pos), B, Q, T,
+                                    _p(scores), _s(stream)), "dsa_indexer_scores")
+
+
+def topk_select(cfg, scores, q_pos, idx, ws=None, stream=None):
+    """scores [B,Q,T] f32, q_pos [B,Q] i32 -> idx [B,Q,topk] i32."""
+    _need(scores, "scores", torch.float32, 3); _need(q_pos, "q_pos", torch.int32, 2)
+    _need(idx, "idx", torch.int32, 3)
+    B, Q, T = scores.shape
+    _check(lib().dsa_topk_select(ctypes.byref(cfg), _p(scores), _p(q_pos), B, Q, T, _p(idx), _p(ws),
+                                 0 if ws is None else ws.numel(), _s(stream)), "dsa_topk_select")
+
+
+def sparse_mla_attn(cfg, q, kv, idx, out, lse=None, ws=None, stream=None):
+    """q [B,Q,64,576] bf16, kv [B,T,576] bf16, idx [B,Q,topk] i32 -> out [B,Q,64,512] bf16 (+ lse [B,Q,64] f32)."""
+    _need(q, "q", torch.bfloat16, 4); _need(kv, "kv", torch.bfloat16, 3); _need(idx, "idx", torch.int32, 3)
+    _need(out, "out", torch.bfloat16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    B, Q, T = q.shape[0], q.shape[1], kv.shape[1]
+    _check(lib().dsa_sparse_mla_attn(ctypes.byref(cfg), _p(q), _p(kv), _p(idx), B, Q, T, _p(out), _p(lse),
+                                     _p(ws), 0 if ws is None else ws.numel(), _s(stream)), "dsa_sparse_mla_attn")
+
+
+def indexshare_group_forward(cfg, q_idx, w, k_idx, q_pos, qs: Sequence[torch.Tensor], kvs: Sequence[torch.Tensor],
+                             outs: Sequence[torch.Tensor], idx_out=None, ws=None, stream=None):
+    """One IndexShare group: one indexer + top-k, then len(qs) attention layers over the same indices."""
+    _need(q_idx, "q_idx", torch.bfloat16, 4); _need(w, "w", torch.float32, 3)
+    _need(k_idx, "k_idx", torch.bfloat16, 3); _need(q_pos, "q_pos", torch.int32, 2)
+    n = len(qs)
+    if len(kvs) != n or len(outs) != n:
+        raise ValueError("qs, kvs and outs must have one tensor per layer")
+    for i in range(n):
+        _need(qs[i], f"q[{i}]", torch.bfloat16, 4); _need(kvs[i], f"kv[{i}]", torch.bfloat16, 3)
+        _need(outs[i], f"out[{i}]", torch.bfloat16, 4)
+    if idx_out is not None:
+        _need(idx_out, "idx_out", torch.int32, 3)
+    B, Q, T = q_idx.shape[0], q_idx.shape[1], k_idx.shape[1]
+    arr = _VP * n
+    qa = arr(*[t.data_ptr() for t in qs])
+    ka = arr(*[t.data_ptr() for t in kvs])
+    oa = arr(*[t.data_ptr() for t in outs])
+    _check(lib().dsa_indexshare_group_forward(ctypes.byref(cfg), _p(q_idx), _p(w), _p(k_idx), _p(q_pos), qa, ka, n,
+                                              B, Q, T, oa, _p(idx_out), _p(ws), 0 if ws is None else ws.numel(),
+                                              _s(stream)), "dsa_indexshare_group_forward")
+
+
+def mtp_draft_attn(cfg, idx0, q_steps, kv, out, ws=None, stream=None):
+    """idx0 [B,1,topk] i32, q_steps [S,B,64,576] bf16, kv [B,T,576] bf16 -> out [S,B,64,512] bf16."""
+    _need(idx0, "idx0", torch.int32, 3); _need(q_steps, "q_steps", torch.bfloat16, 4)
+    _need(kv, "kv", torch.bfloat16, 3); _need(out, "out", torch.bfloat16, 4)
+    S, B, T = q_steps.shape[0], q_steps.shape[1], kv.shape[1]
+    _check(lib().dsa_mtp_draft_attn(ctypes.byref(cfg), _p(idx0), _p(q_steps), _p(kv), S, B, T, _p(out), _p(ws),
+                                    0 if ws is None else ws.numel(), _s(stream)), "dsa_mtp_draft_attn")
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronizes the stream, reads and clears the device error word; returns the status code."""
+    return int(lib().dsa_get_device_error(_s(stream)))
+
+
+def status_string(status: int) -> str:
+    return lib().dsa_status_string(status).decode()
+
+
+def sm_scale() -> float:
+    return 1.0 / math.sqrt(576)

@@ -1,0 +1,448 @@
+// libdsa: C ABI for DSA sparse attention with IndexShare on B300 (sm_103a).
+// Host side: argument validation, workspace layout, TMA descriptors and the
+// launch sequence of each entry point.  Every entry point only enqueues work on
+// the caller's stream; nothing here allocates device memory or synchronizes.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "dsa.h"
+#include "common.cuh"
+#include "indexer.cuh"
+#include "sparse_mla.cuh"
+#include "topk.cuh"
+
+namespace {
+
+using dsa::attn::kMaxLayers;
+
+constexpr int kIdxHeads = 64, kIdxDim = 128, kHeads = 64, kLora = 512, kRope = 64, kMaxTopk = 2048;
+constexpr int kMaxDevices = 64;
+constexpr long long kMaxRowsY = 65535;  // grid.y limit for (chunk, row) launches
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceState {
+  int sms = 0;
+  bool attrs_set = false;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device facts and one-time kernel attributes.  Returns false on a CUDA error.
+bool device_state(DeviceState **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState &s = g_dev[dev];
+  if (!s.attrs_set) {
+    if (cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    bool ok = true;
+    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::indexer::Cfg<1>::kSmemBytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::indexer::Cfg<2>::kSmemBytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::indexer::Cfg<4>::kSmemBytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::attn::sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::attn::kSmemBytes) == cudaSuccess;
+    if (!ok) return false;
+    if (g_encode == nullptr) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    s.attrs_set = true;
+  }
+  *out = &s;
+  return true;
+}
+
+// 2D bf16 tensor map over a row-major [rows, 128] matrix, 128-byte swizzle,
+// box = 64 columns x box_rows rows.
+bool make_tmap_128(CUtensorMap *map, const void *ptr, unsigned long long rows, unsigned box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kIdxDim * 2)};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+dsa_status_t check_config(const dsa_config_t *c) {
+  if (c == nullptr) return DSA_ERR_INVALID_ARG;
+  if (c->n_idx_heads != kIdxHeads || c->idx_dim != kIdxDim || c->kv_lora_rank != kLora || c->rope_dim != kRope ||
+      c->n_heads != kHeads)
+    return DSA_ERR_UNSUPPORTED;
+  if (c->topk < 1 || c->topk > kMaxTopk || c->topk_freq < 1) return DSA_ERR_UNSUPPORTED;
+  if (!(c->sm_scale > 0.0f) || !std::isfinite(c->sm_scale)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+dsa_status_t check_sizes(int B, int Q, int T) {
+  if (B <= 0 || Q <= 0 || T <= 0) return DSA_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(B) * Q;
+  if (rows > kMaxRowsY) return DSA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * T >= (1LL << 31)) return DSA_ERR_INVALID_ARG;    // TMA row coordinate
+  if (rows * kIdxHeads >= (1LL << 31)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Launch shapes and workspace layout (one definition for sizing and launching)
+// ---------------------------------------------------------------------------
+struct TopkShape {
+  int nchunk = 1, chunk = 0;
+};
+
+TopkShape topk_shape(int rows, int T, int sms) {
+  TopkShape s;
+  if (rows >= 2 * sms) {
+    s.nchunk = 1;
+    s.chunk = T;
+    return s;
+  }
+  const int target = 4 * sms;
+  int n = (target + rows - 1) / rows;
+  const int max_chunks = (T + 4095) / 4096;  // chunks of at least 4096 scores
+  n = n < max_chunks ? n : max_chunks;
+  n = n < 1 ? 1 : n;
+  s.chunk = static_cast<int>(align_up((T + n - 1) / n, 1024));
+  s.nchunk = (T + s.chunk - 1) / s.chunk;
+  return s;
+}
+
+struct AttnShape {
+  int nsplit = 1, bps = 1;
+};
+
+AttnShape attn_shape(long long rowsL, int K, int sms) {
+  AttnShape a;
+  const int nblocks = (K + dsa::attn::kBlk - 1) / dsa::attn::kBlk;
+  int ns = 1;
+  if (rowsL < 2LL * sms) ns = static_cast<int>((2LL * sms + rowsL - 1) / rowsL);
+  ns = ns > nblocks ? nblocks : ns;
+  ns = ns > 16 ? 16 : ns;
+  ns = ns < 1 ? 1 : ns;
+  a.bps = (nblocks + ns - 1) / ns;
+  a.nsplit = (nblocks + a.bps - 1) / a.bps;
+  return a;
+}
+
+struct Layout {
+  size_t scores = 0, ghist = 0, counts = 0, idx = 0, part_o = 0, part_ml = 0, total = 0;
+  TopkShape ts;
+};
+
+size_t attn_partial_bytes(long long rowsL, int K, int sms, size_t *ml_bytes) {
+  const AttnShape a = attn_shape(rowsL, K, sms);
+  if (a.nsplit <= 1) {
+    *ml_bytes = 0;
+    return 0;
+  }
+  *ml_bytes = static_cast<size_t>(rowsL) * a.nsplit * kHeads * 2 * sizeof(float);
+  return static_cast<size_t>(rowsL) * a.nsplit * kHeads * kLora * sizeof(float);
+}
+
+Layout layout(int B, int Q, int T, int n_layers, int K, int sms) {
+  Layout L;
+  const long long rows = static_cast<long long>(B) * Q;
+  L.ts = topk_shape(static_cast<int>(rows), T, sms);
+  size_t off = 0;
+  L.scores = off;
+  off = align_up(off + static_cast<size_t>(rows) * T * sizeof(float), 256);
+  L.ghist = off;
+  if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(dsa::topk::kPasses) * rows * dsa::topk::kMaxBins * 4, 256);
+  L.counts = off;
+  if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(rows) * L.ts.nchunk * 2 * 4, 256);
+  L.idx = off;
+  off = align_up(off + static_cast<size_t>(rows) * K * sizeof(int32_t), 256);
+  // partials: the largest need over a single-layer call and an n_layers call
+  size_t ml1 = 0, mln = 0;
+  const size_t po1 = attn_partial_bytes(rows, K, sms, &ml1);
+  const size_t pon = attn_partial_bytes(rows * n_layers, K, sms, &mln);
+  L.part_o = off;
+  off = align_up(off + (po1 > pon ? po1 : pon), 256);
+  L.part_ml = off;
+  off = align_up(off + (ml1 > mln ? ml1 : mln), 256);
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Launch helpers (arguments already validated)
+// ---------------------------------------------------------------------------
+dsa_status_t launch_indexer(const DeviceState &dev, const dsa_bf16_t *q_idx, const float *w, const dsa_bf16_t *k_idx,
+                            const int32_t *q_pos, int B, int Q, int T, float *scores, cudaStream_t stream) {
+  const int QG = Q == 1 ? 1 : (Q == 2 ? 2 : 4);
+  CUtensorMap tk, tq;
+  if (!make_tmap_128(&tk, k_idx, static_cast<unsigned long long>(B) * T, dsa::indexer::kTileKeys)) return DSA_ERR_CUDA;
+  if (!make_tmap_128(&tq, q_idx, static_cast<unsigned long long>(B) * Q * kIdxHeads, QG * kIdxHeads))
+    return DSA_ERR_CUDA;
+  dsa::indexer::Params p;
+  p.w = w;
+  p.q_pos = q_pos;
+  p.scores = scores;
+  p.B = B;
+  p.Q = Q;
+  p.T = T;
+  p.ngroups = (Q + QG - 1) / QG;
+  p.ntiles = (T + dsa::indexer::kTileKeys - 1) / dsa::indexer::kTileKeys;
+  p.units = static_cast<long long>(B) * p.ngroups * p.ntiles;
+  p.stream_keys = p.ngroups == 1 ? 1 : 0;
+  const long long grid = p.units < dev.sms ? p.units : dev.sms;
+  if (QG == 1)
+    dsa::indexer::indexer_scores_kernel<1><<<static_cast<unsigned>(grid), dsa::indexer::kThreads,
+                                              dsa::indexer::Cfg<1>::kSmemBytes, stream>>>(tk, tq, p);
+  else if (QG == 2)
+    dsa::indexer::indexer_scores_kernel<2><<<static_cast<unsigned>(grid), dsa::indexer::kThreads,
+                                              dsa::indexer::Cfg<2>::kSmemBytes, stream>>>(tk, tq, p);
+  else
+    dsa::indexer::indexer_scores_kernel<4><<<static_cast<unsigned>(grid), dsa::indexer::kThreads,
+                                              dsa::indexer::Cfg<4>::kSmemBytes, stream>>>(tk, tq, p);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status_t launch_topk(const Layout &L, uint8_t *ws, const float *scores, const int32_t *q_pos, int rows, int T,
+                         int K, int32_t *idx, cudaStream_t stream) {
+  using namespace dsa::topk;
+  if (L.ts.nchunk == 1) {
+    topk_row_kernel<<<rows, kThreads, 0, stream>>>(scores, q_pos, T, K, idx);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  }
+  ChunkParams p;
+  p.scores = scores;
+  p.q_pos = q_pos;
+  p.T = T;
+  p.K = K;
+  p.rows = rows;
+  p.chunk = L.ts.chunk;
+  p.nchunk = L.ts.nchunk;
+  p.ghist = reinterpret_cast<uint32_t *>(ws + L.ghist);
+  p.counts = reinterpret_cast<uint32_t *>(ws + L.counts);
+  p.idx = idx;
+  if (cudaMemsetAsync(p.ghist, 0, static_cast<size_t>(kPasses) * rows * kMaxBins * 4, stream) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  const dim3 grid(p.nchunk, rows);
+  topk_chunk_hist_kernel<0><<<grid, kThreads, 0, stream>>>(p);
+  topk_chunk_hist_kernel<1><<<grid, kThreads, 0, stream>>>(p);
+  topk_chunk_hist_kernel<2><<<grid, kThreads, 0, stream>>>(p);
+  topk_chunk_count_kernel<<<grid, kThreads, 0, stream>>>(p);
+  topk_chunk_write_kernel<<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+// Attention over n_layers layers (or draft steps) that share one index set.
+dsa_status_t launch_attention(const DeviceState &dev, const Layout &L, uint8_t *ws, const dsa_bf16_t *const *q,
+                              const dsa_bf16_t *const *kv, dsa_bf16_t *const *out, float *const *lse, int n_layers,
+                              const int32_t *idx, int rows, int Q, int T, int K, float sm_scale,
+                              cudaStream_t stream) {
+  dsa::attn::Params p;
+  std::memset(&p, 0, sizeof(p));
+  for (int l = 0; l < n_layers; ++l) {
+    p.q[l] = reinterpret_cast<const __nv_bfloat16 *>(q[l]);
+    p.kv[l] = reinterpret_cast<const __nv_bfloat16 *>(kv[l]);
+    p.out[l] = reinterpret_cast<__nv_bfloat16 *>(out[l]);
+    p.lse[l] = lse ? lse[l] : nullptr;
+  }
+  p.idx = idx;
+  p.n_layers = n_layers;
+  p.Q = Q;
+  p.T = T;
+  p.K = K;
+  p.rows = rows;
+  const AttnShape a = attn_shape(static_cast<long long>(rows) * n_layers, K, dev.sms);
+  p.nsplit = a.nsplit;
+  p.blocks_per_split = a.bps;
+  p.part_o = reinterpret_cast<float *>(ws + L.part_o);
+  p.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  const long long blocks = static_cast<long long>(n_layers) * p.nsplit * rows;
+  dsa::attn::sparse_mla_kernel<<<static_cast<unsigned>(blocks), dsa::attn::kThreads, dsa::attn::kSmemBytes, stream>>>(p);
+  if (p.nsplit > 1) {
+    const dim3 cgrid(kHeads, static_cast<unsigned>(static_cast<long long>(rows) * n_layers));
+    dsa::attn::combine_kernel<<<cgrid, 128, 0, stream>>>(p);
+  }
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+#define DSA_TRY(expr)                 \
+  do {                                \
+    const dsa_status_t s_ = (expr);   \
+    if (s_ != DSA_OK) return s_;      \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+void dsa_config_default(dsa_config_t *cfg) {
+  if (cfg == nullptr) return;
+  cfg->n_idx_heads = kIdxHeads;
+  cfg->idx_dim = kIdxDim;
+  cfg->topk = kMaxTopk;
+  cfg->topk_freq = 4;
+  cfg->kv_lora_rank = kLora;
+  cfg->rope_dim = kRope;
+  cfg->n_heads = kHeads;
+  cfg->sm_scale = 1.0f / std::sqrt(static_cast<float>(kLora + kRope));
+  cfg->index_share_for_mtp = 1;
+}
+
+size_t dsa_workspace_bytes(const dsa_config_t *cfg, int B, int Q, int T, int n_layers) {
+  if (check_config(cfg) != DSA_OK || check_sizes(B, Q, T) != DSA_OK || n_layers < 1 || n_layers > kMaxLayers)
+    return 0;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return 0;
+  return layout(B, Q, T, n_layers, cfg->topk, dev->sms).total;
+}
+
+dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const dsa_bf16_t *q_idx, const float *w,
+                                const dsa_bf16_t *k_idx, const int32_t *q_pos, int B, int Q, int T, float *scores,
+                                dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  DSA_TRY(check_sizes(B, Q, T));
+  if (!q_idx || !w || !k_idx || !q_pos || !scores) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(q_pos) || !aligned16(scores))
+    return DSA_ERR_ALIGNMENT;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  return launch_indexer(*dev, q_idx, w, k_idx, q_pos, B, Q, T, scores, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t dsa_topk_select(const dsa_config_t *cfg, const float *scores, const int32_t *q_pos, int B, int Q, int T,
+                             int32_t *idx, void *ws, size_t ws_bytes, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  DSA_TRY(check_sizes(B, Q, T));
+  if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(scores) || !aligned16(q_pos) || !aligned16(idx) || (ws && !aligned16(ws))) return DSA_ERR_ALIGNMENT;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  const Layout L = layout(B, Q, T, 1, cfg->topk, dev->sms);
+  if (L.ts.nchunk > 1 && (ws == nullptr || ws_bytes < L.total)) return DSA_ERR_WORKSPACE;
+  return launch_topk(L, static_cast<uint8_t *>(ws), scores, q_pos, B * Q, T, cfg->topk, idx,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t dsa_sparse_mla_attn(const dsa_config_t *cfg, const dsa_bf16_t *q, const dsa_bf16_t *kv,
+                                 const int32_t *idx, int B, int Q, int T, dsa_bf16_t *out, float *lse, void *ws,
+                                 size_t ws_bytes, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  DSA_TRY(check_sizes(B, Q, T));
+  if (!q || !kv || !idx || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(idx) || !aligned16(out) || (lse && !aligned16(lse)) ||
+      (ws && !aligned16(ws)))
+    return DSA_ERR_ALIGNMENT;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  const Layout L = layout(B, Q, T, 1, cfg->topk, dev->sms);
+  if (attn_shape(static_cast<long long>(B) * Q, cfg->topk, dev->sms).nsplit > 1 &&
+      (ws == nullptr || ws_bytes < L.total))
+    return DSA_ERR_WORKSPACE;
+  const dsa_bf16_t *qs[1] = {q};
+  const dsa_bf16_t *kvs[1] = {kv};
+  dsa_bf16_t *outs[1] = {out};
+  float *lses[1] = {lse};
+  return launch_attention(*dev, L, static_cast<uint8_t *>(ws), qs, kvs, outs, lses, 1, idx, B * Q, Q, T, cfg->topk,
+                          cfg->sm_scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t dsa_indexshare_group_forward(const dsa_config_t *cfg, const dsa_bf16_t *q_idx, const float *w,
+                                          const dsa_bf16_t *k_idx, const int32_t *q_pos, const dsa_bf16_t *const *q,
+                                          const dsa_bf16_t *const *kv, int n_layers, int B, int Q, int T,
+                                          dsa_bf16_t *const *out, int32_t *idx_out, void *ws, size_t ws_bytes,
+                                          dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  DSA_TRY(check_sizes(B, Q, T));
+  if (n_layers < 1 || n_layers > kMaxLayers) return DSA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * Q * n_layers > kMaxRowsY) return DSA_ERR_INVALID_ARG;
+  if (!q_idx || !w || !k_idx || !q_pos || !q || !kv || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(q_pos) || (idx_out && !aligned16(idx_out)))
+    return DSA_ERR_ALIGNMENT;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!q[l] || !kv[l] || !out[l]) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q[l]) || !aligned16(kv[l]) || !aligned16(out[l])) return DSA_ERR_ALIGNMENT;
+  }
+  if (ws == nullptr) return DSA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return DSA_ERR_ALIGNMENT;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  const Layout L = layout(B, Q, T, n_layers, cfg->topk, dev->sms);
+  if (ws_bytes < L.total) return DSA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  float *scores = reinterpret_cast<float *>(wsb + L.scores);
+  int32_t *idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(wsb + L.idx);
+  // IndexShare: the indexer and top-k run once for the whole group ...
+  DSA_TRY(launch_indexer(*dev, q_idx, w, k_idx, q_pos, B, Q, T, scores, st));
+  DSA_TRY(launch_topk(L, wsb, scores, q_pos, B * Q, T, cfg->topk, idx, st));
+  // ... and every layer of the group attends over the same index set.
+  return launch_attention(*dev, L, wsb, q, kv, out, nullptr, n_layers, idx, B * Q, Q, T, cfg->topk, cfg->sm_scale,
+                          st);
+}
+
+dsa_status_t dsa_mtp_draft_attn(const dsa_config_t *cfg, const int32_t *idx0, const dsa_bf16_t *q_steps,
+                                const dsa_bf16_t *kv, int S, int B, int T, dsa_bf16_t *out, void *ws, size_t ws_bytes,
+                                dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (!cfg->index_share_for_mtp) return DSA_ERR_UNSUPPORTED;
+  DSA_TRY(check_sizes(B, 1, T));
+  if (S < 1 || S > kMaxLayers || static_cast<long long>(S) * B > kMaxRowsY) return DSA_ERR_INVALID_ARG;
+  if (!idx0 || !q_steps || !kv || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(idx0) || !aligned16(q_steps) || !aligned16(kv) || !aligned16(out) || (ws && !aligned16(ws)))
+    return DSA_ERR_ALIGNMENT;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  const Layout L = layout(B, 1, T, S, cfg->topk, dev->sms);
+  if (attn_shape(static_cast<long long>(B) * S, cfg->topk, dev->sms).nsplit > 1 &&
+      (ws == nullptr || ws_bytes < L.total))
+    return DSA_ERR_WORKSPACE;
+  const dsa_bf16_t *qs[kMaxLayers];
+  const dsa_bf16_t *kvs[kMaxLayers];
+  dsa_bf16_t *outs[kMaxLayers];
+  const size_t qstep = static_cast<size_t>(B) * kHeads * (kLora + kRope);
+  const size_t ostep = static_cast<size_t>(B) * kHeads * kLora;
+  for (int s = 0; s < S; ++s) {
+    qs[s] = q_steps + s * qstep;
+    kvs[s] = kv;  // KV share: every draft step reads the target's cache only
+    outs[s] = out + s * ostep;
+  }
+  return launch_attention(*dev, L, static_cast<uint8_t *>(ws), qs, kvs, outs, nullptr, S, idx0, B, 1, T, cfg->topk,
+                          cfg->sm_scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *dsa_status_string(dsa_status_t s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_ALIGNMENT: return "DSA_ERR_ALIGNMENT";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_DEVICE_CHECK: return "DSA_ERR_DEVICE_CHECK";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+dsa_status_t dsa_get_device_error(dsa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
+  unsigned word = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&word, dsa::g_error_word, sizeof(word)) != cudaSuccess) return DSA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(dsa::g_error_word, &zero, sizeof(zero)) != cudaSuccess) return DSA_ERR_CUDA;
+  if (word & dsa::kErrTimeout) return DSA_ERR_TIMEOUT;
+  if (word & dsa::kErrDeviceCheck) return DSA_ERR_DEVICE_CHECK;
+  return DSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,321 @@
+// Lightning Indexer scores on the 5th-generation tensor cores.
+//
+// S[b,t,s] = sum_j w[b,t,j] * ReLU(q_I[b,t,j,:] . k_I[b,s,:]) for s <= pos(b,t)
+// ("GLM-5.2 Explained: 1M Token Context AI Agent Model", §2.1, relevance score
+// I_{t,s} = w . sigma(q_t^T h_s), read with sigma = ReLU per indexer head).
+//
+// One MMA tile puts 128 cached keys on M and the 64 heads of QG query tokens on
+// N (N = 64*QG), K = the 128 indexer dims.  The fp32 tile lands in tensor
+// memory with one key per TMEM lane, so the ReLU and the weighted head sum run
+// inside one thread: no shuffles, no shared-memory round trip.
+//
+// Warp roles (192 threads, one block per SM, persistent over a contiguous
+// range of (sequence, query group, key tile) units):
+//   warp 0     TMA producer: key tiles (two 64-dim halves, 128-byte swizzle)
+//              into a ring of stages; the query-group operand once per group.
+//   warp 1     allocates tensor memory and issues tcgen05.mma (one thread).
+//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes, ReLU, weighted
+//              head sum, one coalesced fp32 store per key and query.
+// Key tiles entirely after every query's position in the group are not
+// loaded; the epilogue writes -inf there.
+#pragma once
+
+#include "common.cuh"
+
+namespace dsa {
+namespace indexer {
+
+constexpr int kHeads = 64;
+constexpr int kDim = 128;
+constexpr int kTileKeys = 128;                     // UMMA M
+constexpr int kHalfABytes = kTileKeys * 64 * 2;    // one 64-dim half of a key tile: 16 KB
+constexpr int kABytes = 2 * kHalfABytes;           // 32 KB per stage
+constexpr int kThreads = 192;
+
+template <int QG>
+struct Cfg {
+  static constexpr int N = QG * kHeads;                 // UMMA N: 64, 128 or 256
+  static constexpr int kHalfBBytes = N * 64 * 2;
+  static constexpr int kBBytes = 2 * kHalfBBytes;
+  static constexpr int kStages = QG == 1 ? 6 : (QG == 2 ? 5 : 4);
+  static constexpr int kAcc = QG == 4 ? 2 : 4;          // accumulator buffers in TMEM
+  static constexpr int kTmemCols = (kAcc * N <= 256) ? 256 : 512;
+  static constexpr int kSmall = 1024 + 4 * QG * kHeads * 4;  // barriers + flags, then per-warp weights
+  static constexpr int kSmemBytes = 1024 + kStages * kABytes + kBBytes + kSmall;
+  static_assert(kAcc * N <= kTmemCols, "accumulators must fit the allocation");
+};
+
+struct Params {
+  const float *w;        // [B, Q, 64]
+  const int32_t *q_pos;  // [B, Q]
+  float *scores;         // [B, Q, T]
+  int B, Q, T;
+  int ngroups;           // ceil(Q / QG)
+  int ntiles;            // ceil(T / 128)
+  long long units;       // B * ngroups * ntiles
+  int stream_keys;       // 1: every key tile is read once (evict-first in L2)
+};
+
+// Largest visible position of a query group (-1 if none), clamped to [-1, T-1].
+template <int QG>
+__device__ __forceinline__ int group_max_pos(const Params &p, int b, int q0) {
+  int m = -1;
+#pragma unroll
+  for (int i = 0; i < QG; ++i) {
+    if (q0 + i < p.Q) {
+      int pos = __ldg(p.q_pos + (size_t)b * p.Q + q0 + i);
+      pos = pos < 0 ? -1 : (pos >= p.T ? p.T - 1 : pos);
+      m = pos > m ? pos : m;
+    }
+  }
+  return m;
+}
+
+template <int QG>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_scores_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                          const Params p) {
+  using C = Cfg<QG>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = base;                                   // [kStages][2 halves][128 rows][128 B]
+  uint8_t *sB = base + C::kStages * kABytes;            // [2 halves][N rows][128 B]
+  uint8_t *small = sB + C::kBBytes;
+  uint64_t *full = reinterpret_cast<uint64_t *>(small);
+  uint64_t *empty = full + C::kStages;
+  uint64_t *tfull = empty + C::kStages;
+  uint64_t *tempty = tfull + C::kAcc;
+  uint64_t *bfull = tempty + C::kAcc;
+  uint64_t *bfree = bfull + 1;
+  uint64_t *mma_done = bfree + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  // [4 epilogue warps][QG][64]: each epilogue warp keeps its own copy of the
+  // current group's head weights, so the warps never wait on one another.
+  float *sw_all = reinterpret_cast<float *>(small + 1024);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const long long u_begin = p.units * blockIdx.x / gridDim.x;
+  const long long u_end = p.units * (blockIdx.x + 1) / gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < C::kAcc; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    mbar_init(bfull, 1);
+    mbar_init(bfree, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_q);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      long long cur_seg = -1;
+      int seg_max = -1;
+      uint32_t b_loads = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      for (long long u = u_begin; u < u_end && !*abort_flag; ++u) {
+        const long long seg = u / p.ntiles;
+        const int tile = static_cast<int>(u - seg * p.ntiles);
+        const int b = static_cast<int>(seg / p.ngroups);
+        const int q0 = static_cast<int>(seg - (long long)b * p.ngroups) * QG;
+        if (seg != cur_seg) seg_max = group_max_pos<QG>(p, b, q0);
+        if (tile * kTileKeys > seg_max) continue;  // fully masked tile: no load
+        if (seg != cur_seg) {
+          if (b_loads > 0 && !mbar_wait_bounded(bfree, (b_loads - 1) & 1u, abort_flag)) break;
+          mbar_arrive_expect_tx(bfull, C::kBBytes);
+          const int yq = (b * p.Q + q0) * kHeads;
+          tma_load_2d(sB, &tmap_q, 0, yq, bfull);
+          tma_load_2d(sB + C::kHalfBBytes, &tmap_q, 64, yq, bfull);
+          ++b_loads;
+          cur_seg = seg;
+        }
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(&full[stage], kABytes);
+        const int yk = b * p.T + tile * kTileKeys;
+        uint8_t *dst = sA + stage * kABytes;
+        if (p.stream_keys) {
+          tma_load_2d_hint(dst, &tmap_k, 0, yk, &full[stage], policy);
+          tma_load_2d_hint(dst + kHalfABytes, &tmap_k, 64, yk, &full[stage], policy);
+        } else {
+          tma_load_2d(dst, &tmap_k, 0, yk, &full[stage]);
+          tma_load_2d(dst + kHalfABytes, &tmap_k, 64, yk, &full[stage]);
+        }
+        issued_mask |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      // Every copy this block issued has landed before the block may exit.
+      for (int s = 0; s < C::kStages; ++s)
+        if (issued_mask & (1u << s)) mbar_wait_drain(&full[s], (issued_parity >> s) & 1u, kWaitLimitNs);
+      if (b_loads > 0) mbar_wait_drain(bfull, (b_loads - 1) & 1u, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc_idesc_bf16(kTileKeys, C::N);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      long long cur_seg = -1;
+      int seg_max = -1;
+      uint32_t b_waits = 0;
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      for (long long u = u_begin; u < u_end && !*abort_flag; ++u) {
+        const long long seg = u / p.ntiles;
+        const int tile = static_cast<int>(u - seg * p.ntiles);
+        const int b = static_cast<int>(seg / p.ngroups);
+        const int q0 = static_cast<int>(seg - (long long)b * p.ngroups) * QG;
+        if (seg != cur_seg) seg_max = group_max_pos<QG>(p, b, q0);
+        if (tile * kTileKeys > seg_max) continue;
+        if (seg != cur_seg) {
+          if (b_waits > 0) tc_commit(bfree);  // previous group's operand is free once its MMAs finish
+          if (!mbar_wait_bounded(bfull, b_waits & 1u, abort_flag)) break;
+          ++b_waits;
+          cur_seg = seg;
+        }
+        if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
+        if (!mbar_wait_bounded(&full[stage], phase, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::N);
+        const uint32_t a_stage = a0 + stage * kABytes;
+#pragma unroll
+        for (int kk = 0; kk < kDim / 16; ++kk) {
+          const uint32_t koff = (kk & 3) * 32u;  // K=16 step inside a 128-byte swizzled row
+          const uint64_t ad = tc_desc_sw128(a_stage + (kk >> 2) * kHalfABytes + koff);
+          const uint64_t bd = tc_desc_sw128(b0 + (kk >> 2) * C::kHalfBBytes + koff);
+          tc_mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&empty[stage]);
+        tc_commit(&tfull[acc]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++acc == C::kAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // All MMAs issued by this thread are complete before tensor memory is freed.
+      tc_commit(mma_done);
+      mbar_wait_drain(mma_done, 0, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;                  // TMEM lanes this warp may read
+    float *sw = sw_all + (warp - 2) * QG * kHeads;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    long long cur_seg = -1;
+    int seg_max = -1;
+    int posv[QG];
+    int b = 0, q0 = 0;
+    for (long long u = u_begin; u < u_end; ++u) {
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const long long seg = u / p.ntiles;
+      const int tile = static_cast<int>(u - seg * p.ntiles);
+      if (seg != cur_seg) {
+        b = static_cast<int>(seg / p.ngroups);
+        q0 = static_cast<int>(seg - (long long)b * p.ngroups) * QG;
+        seg_max = group_max_pos<QG>(p, b, q0);
+        __syncwarp();  // the warp is done with the previous group's weights
+        for (int i = lane; i < QG * kHeads; i += 32) {
+          const int q = q0 + i / kHeads;
+          sw[i] = q < p.Q ? __ldg(p.w + ((size_t)b * p.Q + q) * kHeads + (i % kHeads)) : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < QG; ++i) {
+          int pos = (q0 + i < p.Q) ? __ldg(p.q_pos + (size_t)b * p.Q + q0 + i) : -1;
+          if (q0 + i < p.Q && (pos < 0 || pos >= p.T) && warp == 2 && lane == 0 && tile == 0)
+            raise_error(kErrDeviceCheck);
+          posv[i] = pos < 0 ? -1 : (pos >= p.T ? p.T - 1 : pos);
+        }
+        __syncwarp();
+        cur_seg = seg;
+      }
+      const int key = tile * kTileKeys + quarter * 32 + lane;
+      const bool real = tile * kTileKeys <= seg_max;
+      if (real) {
+        // One lane polls; the verdict is shared so the whole warp either
+        // proceeds to the warp-collective TMEM loads or leaves together.
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int i = 0; i < QG; ++i) {
+        if (q0 + i >= p.Q) break;
+        float s = 0.0f;
+        if (real) {
+          const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * C::N + i * kHeads);
+          const float4 *w4 = reinterpret_cast<const float4 *>(sw + i * kHeads);
+          float v[32];
+          float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_ld_32x32b_x32(taddr + h * 32, v);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              const float4 wv = w4[(h * 32 + j) >> 2];
+              s0 = fmaf(wv.x, fmaxf(v[j + 0], 0.0f), s0);
+              s1 = fmaf(wv.y, fmaxf(v[j + 1], 0.0f), s1);
+              s0 = fmaf(wv.z, fmaxf(v[j + 2], 0.0f), s0);
+              s1 = fmaf(wv.w, fmaxf(v[j + 3], 0.0f), s1);
+            }
+          }
+          s = s0 + s1;
+        }
+        if (key < p.T) {
+          float *row = p.scores + ((size_t)b * p.Q + q0 + i) * (size_t)p.T;
+          row[key] = (real && key <= posv[i]) ? s : -INFINITY;
+        }
+      }
+      if (real) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (++acc == C::kAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace indexer
+}  // namespace dsa

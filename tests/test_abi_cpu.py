@@ -1,0 +1,80 @@
+"""CPU-side checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from long_context_sparse_26_b300 import binding
+from long_context_sparse_26_b300.build import LIB, build_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_library()
+    assert os.path.exists(LIB)
+    return binding.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("dsa_indexer_scores", "dsa_topk_select", "dsa_sparse_mla_attn", "dsa_indexshare_group_forward",
+                 "dsa_mtp_draft_attn", "dsa_workspace_bytes", "dsa_status_string", "dsa_get_device_error"):
+        assert name in syms
+    assert set(syms) <= set(binding.EXPORTS) | {"dsa_config_default"}
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_default_config(L):
+    cfg = binding.default_config()
+    assert (cfg.n_idx_heads, cfg.idx_dim, cfg.topk, cfg.topk_freq, cfg.kv_lora_rank, cfg.rope_dim, cfg.n_heads,
+            cfg.index_share_for_mtp) == (64, 128, 2048, 4, 512, 64, 64, 1)
+    assert abs(cfg.sm_scale - 576 ** -0.5) < 1e-7
+
+
+def test_status_strings(L):
+    assert binding.status_string(0) == "DSA_OK"
+    assert binding.status_string(7) == "DSA_ERR_TIMEOUT"
+
+
+def _call_scores(L, cfg, ptrs, B=1, Q=1, T=16):
+    return L.dsa_indexer_scores(ctypes.byref(cfg), *[ctypes.c_void_p(p) for p in ptrs[:4]], B, Q, T,
+                                ctypes.c_void_p(ptrs[4]), None)
+
+
+def test_host_validation_rejects_before_launch(L):
+    cfg = binding.default_config()
+    good = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000]   # never dereferenced: validation fails first
+    bad_cfg = binding.default_config()
+    bad_cfg.n_heads = 32
+    assert _call_scores(L, bad_cfg, good) == 2            # unsupported shape constant
+    bad_cfg = binding.default_config()
+    bad_cfg.topk = 4096
+    assert _call_scores(L, bad_cfg, good) == 2
+    bad_cfg = binding.default_config()
+    bad_cfg.sm_scale = -1.0
+    assert _call_scores(L, bad_cfg, good) == 1
+    assert _call_scores(L, cfg, [0] + good[1:]) == 1     # null pointer
+    assert _call_scores(L, cfg, good, B=0) == 1           # empty batch
+    assert _call_scores(L, cfg, good, T=-5) == 1
+    assert _call_scores(L, cfg, good, B=70000) == 1       # rows beyond the launch limit
+    assert _call_scores(L, cfg, [0x1008] + good[1:]) == 3  # misaligned
+    assert L.dsa_indexshare_group_forward(ctypes.byref(cfg), *[ctypes.c_void_p(p) for p in good[:4]], None, None, 9,
+                                          1, 1, 16, None, None, None, 0, None) == 1   # 9 layers > 8
+    cfg_nomtp = binding.default_config()
+    cfg_nomtp.index_share_for_mtp = 0
+    assert L.dsa_mtp_draft_attn(ctypes.byref(cfg_nomtp), *[ctypes.c_void_p(p) for p in good[:3]], 7, 1, 16,
+                                ctypes.c_void_p(good[4]), None, 0, None) == 2

@@ -1,0 +1,340 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Small seeded cases span several tiles and a ragged tail; edge cases cover
+ties, short rows (-1 padding), masked positions and bad indices.  Tolerances
+are in tests/parity.py.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_sparse_26_b300 import binding as dsa
+from long_context_sparse_26_b300 import workloads as wl
+from parity import check_attention, check_scores_row, check_topk_row, f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+SCALE = wl.SM_SCALE
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from long_context_sparse_26_b300.build import build_library
+    build_library()
+    dsa.lib()
+    yield
+    assert dsa.get_device_error() == 0
+
+
+def _indexer_inputs(B, Q, T, first_pos, seed):
+    q_idx = wl.indexer_queries(B, Q, seed, DEV)
+    w = wl.head_weights(B, Q, seed, DEV)
+    k_idx = wl.indexer_keys(B, T, seed, DEV)
+    pos = torch.arange(first_pos, first_pos + Q, dtype=torch.int32, device=DEV).unsqueeze(0).repeat(B, 1)
+    return q_idx, w, k_idx, pos.contiguous()
+
+
+# --------------------------------------------------------------------------- a1: indexer scores
+
+@pytest.mark.parametrize("B,Q,T,first", [
+    (2, 1, 3000, 2999),      # decode, N=64, ragged last tile
+    (1, 2, 1000, 998),       # two queries per group (N=128)
+    (1, 4, 2500, 2496),      # four queries per group (N=256)
+    (2, 5, 700, 300),        # ragged query group, masked tail tiles
+    (1, 9, 4100, 4000),      # several groups, causal
+    (3, 1, 128, 127),        # exactly one tile
+])
+def test_indexer_scores(B, Q, T, first):
+    cfg = dsa.default_config()
+    q_idx, w, k_idx, pos = _indexer_inputs(B, Q, T, first, seed=11 + T)
+    scores = torch.full((B, Q, T), float("nan"), device=DEV)
+    dsa.indexer_scores(cfg, q_idx, w, k_idx, pos, scores)
+    torch.cuda.synchronize()
+    ora = oracle.indexer_scores(f64(q_idx), f64(w), f64(k_idx), pos.cpu().numpy())
+    g = scores.cpu().double().numpy()
+    for b in range(B):
+        for t in range(Q):
+            check_scores_row(g[b, t], ora[b, t], int(pos[b, t]))
+
+
+def test_indexer_signed_weights_and_exact_zero():
+    """Negative head weights are allowed; keys orthogonal to every head give 0."""
+    cfg = dsa.default_config()
+    B, Q, T = 1, 1, 640
+    q_idx, w, k_idx, pos = _indexer_inputs(B, Q, T, T - 1, seed=5)
+    w = (w - 0.5 / 64).contiguous()
+    k_idx[0, 100:140] = 0
+    scores = torch.empty(B, Q, T, device=DEV)
+    dsa.indexer_scores(cfg, q_idx, w, k_idx, pos, scores)
+    ora = oracle.indexer_scores(f64(q_idx), f64(w), f64(k_idx), pos.cpu().numpy())
+    g = scores.cpu().double().numpy()
+    assert np.all(g[0, 0, 100:140] == 0.0)
+    err = np.abs(g[0, 0] - ora[0, 0])
+    assert err.max() <= 2e-3 * np.abs(ora[0, 0]).max()
+
+
+# --------------------------------------------------------------------------- a2: top-k
+
+def _topk_case(scores_np, pos_np, k):
+    cfg = dsa.default_config(topk=k)
+    B, Q, T = scores_np.shape
+    scores = torch.from_numpy(scores_np.astype(np.float32)).to(DEV)
+    pos = torch.from_numpy(pos_np.astype(np.int32)).to(DEV)
+    idx = torch.full((B, Q, k), -7, dtype=torch.int32, device=DEV)
+    ws = dsa.alloc_workspace(cfg, B, Q, T, 1)
+    dsa.topk_select(cfg, scores, pos, idx, ws)
+    torch.cuda.synchronize()
+    # the oracle sorts the same fp32 values (exactly representable in fp64)
+    ora = oracle.topk_select(scores_np.astype(np.float32).astype(np.float64), pos_np, k)
+    return idx.cpu().numpy(), ora
+
+
+@pytest.mark.parametrize("B,Q,T,k,kind", [
+    (2, 1, 100_000, 2048, "normal"),     # few long rows: chunked path
+    (1, 3, 70_001, 2048, "ints"),        # heavy exact ties
+    (1, 2, 50_000, 2048, "equal"),       # every score equal: pure tie-break
+    (1, 320, 5000, 2048, "normal"),      # many rows: one block per row
+    (1, 320, 3000, 700, "ints"),
+    (4, 1, 9000, 7, "normal"),           # tiny k
+    (2, 2, 1500, 2048, "normal"),        # L < k: -1 padding
+])
+def test_topk_bit_exact(B, Q, T, k, kind):
+    rng = np.random.default_rng(T + k)
+    if kind == "normal":
+        s = rng.standard_normal((B, Q, T))
+    elif kind == "ints":
+        s = rng.integers(0, 50, (B, Q, T)).astype(np.float64)
+    else:
+        s = np.full((B, Q, T), 0.25)
+    s[..., ::97] = -s[..., ::97]            # negative scores too
+    s[..., 5] = 0.0
+    s[..., 6] = -0.0                       # -0 and +0 tie
+    pos = rng.integers(max(0, T - 3000), T, (B, Q))
+    pos[0, 0] = T - 1
+    g, o = _topk_case(s, pos, k)
+    assert np.array_equal(g, o)
+
+
+def test_topk_short_and_empty_rows():
+    s = np.random.default_rng(0).standard_normal((1, 4, 4096))
+    pos = np.array([[0, 10, 2047, 2048]])
+    g, o = _topk_case(s, pos, 2048)
+    assert np.array_equal(g, o)
+    assert list(g[0, 0, :2]) == [0, -1]
+
+
+# --------------------------------------------------------------------------- a3: sparse attention
+
+def _attn_inputs(B, Q, T, k, seed, pad=0):
+    q = wl.mla_queries(B, Q, seed, 0, DEV)
+    kv = wl.latent_cache(B, T, seed, 0, DEV)
+    rng = np.random.default_rng(seed)
+    idx = np.full((B, Q, k), -1, dtype=np.int32)
+    for b in range(B):
+        for t in range(Q):
+            n = k - pad if k - pad <= T else T
+            idx[b, t, :n] = np.sort(rng.choice(T, n, replace=False))
+    return q, kv, torch.from_numpy(idx).to(DEV)
+
+
+@pytest.mark.parametrize("B,Q,T,k,pad", [
+    (1, 1, 5000, 2048, 0),       # one row: many splits
+    (2, 2, 9000, 2048, 37),      # padding slots
+    (3, 1, 3000, 100, 0),        # ragged last block
+    (1, 1, 40, 2048, 0),         # fewer rows than slots
+    (40, 8, 2500, 256, 0),       # many rows: single split, no combine
+])
+def test_sparse_attention(B, Q, T, k, pad):
+    cfg = dsa.default_config(topk=k)
+    q, kv, idx = _attn_inputs(B, Q, T, k, seed=B * 1000 + T, pad=pad)
+    out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, Q, 64, dtype=torch.float32, device=DEV)
+    ws = dsa.alloc_workspace(cfg, B, Q, T, 1)
+    dsa.sparse_mla_attn(cfg, q, kv, idx, out, lse, ws)
+    torch.cuda.synchronize()
+    O, LSE = oracle.sparse_mla_attn(f64(q), f64(kv), idx.cpu().numpy(), SCALE)
+    check_attention(f64(out), O)
+    assert np.abs(lse.cpu().double().numpy() - LSE).max() < 1e-3
+
+
+def test_attention_one_hot_and_empty_rows():
+    cfg = dsa.default_config(topk=64)
+    B, Q, T = 1, 2, 300
+    kv = wl.latent_cache(B, T, 3, 0, DEV)
+    q = torch.zeros(B, Q, 64, 576, dtype=torch.bfloat16, device=DEV)
+    q[0, 0] = (kv[0, 123].float() * 0.5).to(torch.bfloat16)   # logit at row 123 dominates
+    idx = torch.full((B, Q, 64), -1, dtype=torch.int32, device=DEV)
+    idx[0, 0, :5] = torch.tensor([3, 50, 123, 200, 299], dtype=torch.int32)
+    out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, Q, 64, device=DEV)
+    dsa.sparse_mla_attn(cfg, q, kv, idx, out, lse, dsa.alloc_workspace(cfg, B, Q, T, 1))
+    torch.cuda.synchronize()
+    O, _ = oracle.sparse_mla_attn(f64(q), f64(kv), idx.cpu().numpy(), SCALE)
+    check_attention(f64(out), O)
+    assert torch.all(out[0, 1] == 0)                         # no valid index: zeros
+    assert torch.all(torch.isneginf(lse[0, 1]))
+
+
+def test_bad_index_is_reported_not_faulted():
+    cfg = dsa.default_config(topk=64)
+    B, Q, T = 1, 1, 100
+    q, kv, idx = _attn_inputs(B, Q, T, 64, seed=1)
+    idx[0, 0, 3] = T + 5
+    out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+    dsa.sparse_mla_attn(cfg, q, kv, idx, out, None, dsa.alloc_workspace(cfg, B, Q, T, 1))
+    assert dsa.get_device_error() == 6
+    assert dsa.get_device_error() == 0        # cleared by the read
+
+
+# --------------------------------------------------------------------------- a4/a6: group and MTP
+
+def _group_check(w_, B=None, T=None, rows=None):
+    """Runs one group through the ABI and checks sampled rows against the oracle."""
+    cfg = dsa.default_config(topk=w_.topk)
+    inp = wl.make_inputs(w_, DEV, B=B, T=T)
+    B, Q, T = inp.q_idx.shape[0], inp.q_idx.shape[1], inp.k_idx.shape[1]
+    outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV) for _ in range(w_.n_layers)]
+    idx = torch.empty(B, Q, w_.topk, dtype=torch.int32, device=DEV)
+    ws = dsa.alloc_workspace(cfg, B, Q, T, w_.n_layers)
+    dsa.indexshare_group_forward(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, inp.q, inp.kv, outs, idx, ws)
+    torch.cuda.synchronize()
+    rows = rows if rows is not None else [(b, t) for b in range(B) for t in range(Q)]
+    g_idx = idx.cpu().numpy()
+    ties = 0
+    for (b, t) in rows:
+        pos = int(inp.q_pos[b, t])
+        S = oracle.indexer_scores_row(f64(inp.q_idx[b, t]), f64(inp.w[b, t]), f64(inp.k_idx[b]), pos)
+        o_idx = oracle.topk_select_row(S, pos, w_.topk)
+        ties += check_topk_row(g_idx[b, t], o_idx, S, pos, w_.topk)
+        for layer in range(w_.n_layers):
+            # attention over the oracle's own index set, gathering only those rows
+            valid = o_idx[o_idx >= 0]
+            rows_kv = f64(inp.kv[layer][b, torch.from_numpy(valid).to(DEV)])
+            O, _ = oracle.sparse_mla_attn_row(f64(inp.q[layer][b, t]), rows_kv, np.arange(valid.size), SCALE)
+            if np.array_equal(g_idx[b, t], o_idx):
+                check_attention(f64(outs[layer][b, t]), O)
+            else:
+                # boundary ties swap a few rows: compare with the oracle on the GPU's set
+                gv = g_idx[b, t][g_idx[b, t] >= 0]
+                rows_g = f64(inp.kv[layer][b, torch.from_numpy(gv).to(DEV)])
+                Og, _ = oracle.sparse_mla_attn_row(f64(inp.q[layer][b, t]), rows_g, np.arange(gv.size), SCALE)
+                check_attention(f64(outs[layer][b, t]), Og)
+    return ties
+
+
+def test_group_tiny_decode():
+    _group_check(wl.TINY)
+
+
+def test_group_equals_four_independent_layers():
+    """North-star check (b) on the GPU: the group call equals four single-layer
+    calls fed the group's index set, bit for bit."""
+    w_ = wl.TINY
+    cfg = dsa.default_config()
+    inp = wl.make_inputs(w_, DEV)
+    B, Q, T = 1, 4, w_.T
+    outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV) for _ in range(4)]
+    idx = torch.empty(B, Q, 2048, dtype=torch.int32, device=DEV)
+    ws = dsa.alloc_workspace(cfg, B, Q, T, 4)
+    dsa.indexshare_group_forward(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, inp.q, inp.kv, outs, idx, ws)
+    ws1 = dsa.alloc_workspace(cfg, B, Q, T, 4)
+    for layer in range(4):
+        single = torch.empty_like(outs[layer])
+        dsa.sparse_mla_attn(cfg, inp.q[layer], inp.kv[layer], idx, single, None, ws1)
+        # the group launch may split the slots differently: compare within rounding
+        d = (single.float() - outs[layer].float()).abs().max().item()
+        assert d <= 4e-3, d
+    # and the group's index set is the standalone indexer + top-k
+    scores = torch.empty(B, Q, T, device=DEV)
+    dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores)
+    idx2 = torch.empty_like(idx)
+    dsa.topk_select(cfg, scores, inp.q_pos, idx2, ws1)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx2)
+
+
+def test_group_is_deterministic():
+    w_ = wl.TINY
+    cfg = dsa.default_config()
+    inp = wl.make_inputs(w_, DEV)
+    res = []
+    for _ in range(2):
+        outs = [torch.empty(1, 4, 64, 512, dtype=torch.bfloat16, device=DEV) for _ in range(4)]
+        idx = torch.empty(1, 4, 2048, dtype=torch.int32, device=DEV)
+        dsa.indexshare_group_forward(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, inp.q, inp.kv, outs, idx,
+                                     dsa.alloc_workspace(cfg, 1, 4, w_.T, 4))
+        res.append((idx.clone(), [o.clone() for o in outs]))
+    torch.cuda.synchronize()
+    assert torch.equal(res[0][0], res[1][0])
+    for a, b in zip(res[0][1], res[1][1]):
+        assert torch.equal(a, b)
+
+
+def test_mtp_draft_small():
+    cfg = dsa.default_config()
+    B, T, S = 3, 6000, 7
+    kv = wl.latent_cache(B, T, 9, 0, DEV)
+    q_steps = wl.draft_queries(S, B, 9, DEV)
+    rng = np.random.default_rng(9)
+    idx0 = np.stack([np.sort(rng.choice(T, 2048, replace=False)) for _ in range(B)])[:, None, :].astype(np.int32)
+    idx0_t = torch.from_numpy(idx0).to(DEV)
+    out = torch.empty(S, B, 64, 512, dtype=torch.bfloat16, device=DEV)
+    dsa.mtp_draft_attn(cfg, idx0_t, q_steps, kv, out, dsa.alloc_workspace(cfg, B, 1, T, S))
+    torch.cuda.synchronize()
+    O = oracle.mtp_draft_attn(idx0, f64(q_steps), f64(kv), SCALE)
+    check_attention(f64(out), O)
+    # one step at a time gives the same result
+    one = torch.empty(1, B, 64, 512, dtype=torch.bfloat16, device=DEV)
+    dsa.mtp_draft_attn(cfg, idx0_t, q_steps[2:3].contiguous(), kv, one, dsa.alloc_workspace(cfg, B, 1, T, 1))
+    torch.cuda.synchronize()
+    assert (one[0].float() - out[2].float()).abs().max().item() <= 4e-3
+
+
+# --------------------------------------------------------------------------- full-size workloads (sampled rows)
+
+def test_full_decode_128k_sampled():
+    _group_check(wl.DECODE_128K, rows=[(0, 0), (17, 0), (31, 0)])
+    torch.cuda.empty_cache()
+
+
+def test_full_decode_1m_sampled():
+    ties = _group_check(wl.DECODE_1M, rows=[(0, 0), (7, 0)])
+    print("boundary ties at 1M:", ties)
+    torch.cuda.empty_cache()
+
+
+def test_full_prefill_sampled():
+    _group_check(wl.PREFILL, rows=[(0, 0), (0, 1), (0, 2049), (0, 4095)])
+    torch.cuda.empty_cache()
+
+
+def test_full_mtp_sampled():
+    w_ = wl.MTP
+    cfg = dsa.default_config()
+    inp = wl.make_inputs(w_, DEV)
+    B, T = w_.B, w_.T
+    scores = torch.empty(B, 1, T, device=DEV)
+    idx0 = torch.empty(B, 1, 2048, dtype=torch.int32, device=DEV)
+    ws = dsa.alloc_workspace(cfg, B, 1, T, w_.mtp_steps)
+    dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores)
+    dsa.topk_select(cfg, scores, inp.q_pos, idx0, ws)
+    out = torch.empty(w_.mtp_steps, B, 64, 512, dtype=torch.bfloat16, device=DEV)
+    dsa.mtp_draft_attn(cfg, idx0, inp.q_steps, inp.kv[0], out, ws)
+    torch.cuda.synchronize()
+    g_idx = idx0.cpu().numpy()
+    for b in (0, 63):
+        S = oracle.indexer_scores_row(f64(inp.q_idx[b, 0]), f64(inp.w[b, 0]), f64(inp.k_idx[b]), T - 1)
+        o_idx = oracle.topk_select_row(S, T - 1, 2048)
+        check_topk_row(g_idx[b, 0], o_idx, S, T - 1, 2048)
+        gv = g_idx[b, 0]
+        rows = f64(inp.kv[0][b, torch.from_numpy(gv).to(DEV)])
+        for s in range(w_.mtp_steps):
+            O, _ = oracle.sparse_mla_attn_row(f64(inp.q_steps[s, b]), rows, np.arange(gv.size), SCALE)
+            check_attention(f64(out[s, b]), O)
+    torch.cuda.empty_cache()
