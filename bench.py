@@ -23,7 +23,6 @@ import math
 import os
 import statistics
 import sys
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -69,58 +68,65 @@ def indexer_flops(w: wl.Workload, B: int) -> int:
 
 
 class ClockSampler:
-    """Polls NVML (read-only) for the SM clock and clock-event reasons."""
+    """Samples SM clocks and clock-event reasons with nvidia-smi (read-only)
+    every 100 ms in a background process."""
 
-    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
-               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int, period_s: float = 0.01):
-        self.samples = []
-        self.period = period_s
-        self._stop = threading.Event()
-        self._mark = None
+    def __init__(self, device_id):
+        import subprocess
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        self.t_start = time.perf_counter()
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception:  # NVML unavailable: no clock record
-            self.nv = None
-            self.max_mhz = None
-        self.t = threading.Thread(target=self._run, daemon=True)
-
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
-                reasons = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                self.samples.append((time.perf_counter(), mhz, reasons))
-            except Exception:
-                pass
-            time.sleep(self.period)
-
-    def start(self):
-        if self.nv is not None:
-            self.t.start()
-        return self
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={device_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
 
     def stop(self):
-        self._stop.set()
-        if self.nv is not None:
-            self.t.join()
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait()
+            self.f.close()
 
     def summary(self, t0: float, t1: float) -> dict:
-        if self.nv is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
-        inside = [s for s in self.samples if t0 <= s[0] <= t1] or self.samples
-        mhz = [s[1] for s in inside]
-        bits = 0
-        for s in inside:
-            bits |= s[2]
-        reasons = [name for bit, name in self.REASONS.items() if bits & bit]
-        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(inside)}
+        """Samples taken between t0 and t1 (perf_counter), counting ~100 ms per sample from the start."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        lo, hi = int((t0 - self.t_start) / 0.1), int((t1 - self.t_start) / 0.1) + 1
+        inside = rows[max(0, lo):max(lo + 1, hi)] or rows
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        mhz = [v for v in (num(r[1]) for r in inside) if v is not None]
+        power = [v for v in (num(r[3]) for r in inside) if v is not None]
+        reasons = set()
+        for r in inside:
+            for name, val in (("hw_slowdown", r[5]), ("hw_thermal_slowdown", r[6]), ("sw_thermal_slowdown", r[7]),
+                              ("sw_power_cap", r[8])):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(inside), "power_w_max": max(power) if power else None}
 
 
 def count_graph_kernels(graph) -> int | None:
@@ -309,11 +315,19 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
     if status != 0:
         raise RuntimeError(f"device error before timing: {dsa.status_string(status)}")
 
-    clocks = ClockSampler(local).start()
+    vis = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    clocks = ClockSampler(vis[local] if local < len(vis) else local)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             graph.replay()
     stream.synchronize()
+    # untimed load so the clock record holds samples taken under this load
+    t_settle = time.perf_counter()
+    with torch.cuda.stream(stream):
+        while time.perf_counter() - t_settle < args.settle:
+            for _ in range(20):
+                graph.replay()
+            stream.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
@@ -375,7 +389,7 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
         step_roof["frac_of_roofline_time"] = step_roof["roofline_ms"] / ms_per_step
 
     # ---- end to end through the public API with host buffers
-    e2e = run_e2e(args, w, cfg, inp, outs, idx, scores, ws, stream, dsa)
+    e2e = None if args.no_e2e else run_e2e(args, w, cfg, inp, outs, idx, scores, ws, stream, dsa)
 
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -389,7 +403,7 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
         "e2e": e2e,
         "gpu_launches": (launches_per_step or 0) * args.steps,
         "gpu_launches_per_step": launches_per_step,
-        "clocks": clocks.summary(t_wall0, t_wall1),
+        "clocks": clocks.summary(t_settle, t_wall1),
         "step_ms_median": statistics.median(step_ms),
     }
     if w.name == wl.DECODE_1M.name and not args.no_variant:
@@ -511,6 +525,51 @@ def run_reference(args, w: wl.Workload) -> dict:
     }
 
 
+def profile_kernel(args, w: wl.Workload):
+    """Runs one entry point a few times on the workload (optionally a smaller
+    batch) with nothing else on the GPU: the small case for ncu captures."""
+    from long_context_sparse_26_b300 import binding as dsa
+    from long_context_sparse_26_b300.build import build_library
+    build_library()
+    dev = "cuda"
+    cfg = dsa.default_config(topk=w.topk)
+    B, Q, T = w.B, w.Q, w.T
+    q_pos = torch.arange(w.first_pos, w.first_pos + Q, dtype=torch.int32, device=dev).repeat(B, 1).contiguous()
+    n_att = w.mtp_steps if w.kind == "mtp" else w.n_layers
+    ws = dsa.alloc_workspace(cfg, B, Q, T, n_att, dev)
+    scores = torch.empty(B, Q, T, device=dev)
+    idx = torch.empty(B, Q, w.topk, dtype=torch.int32, device=dev)
+    kind = args.profile_kernel
+    if kind in ("indexer", "topk", "group"):
+        q_idx = wl.indexer_queries(B, Q, w.seed, dev)
+        wt = wl.head_weights(B, Q, w.seed, dev)
+        k_idx = wl.indexer_keys(B, T, w.seed, dev)
+    if kind == "topk":
+        dsa.indexer_scores(cfg, q_idx, wt, k_idx, q_pos, scores)
+    if kind in ("attention", "group"):
+        q = [wl.mla_queries(B, Q, w.seed, layer, dev) for layer in range(n_att)]
+        kv = [wl.latent_cache(B, T, w.seed, layer, dev) for layer in range(n_att if w.kind != "mtp" else 1)]
+        outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(n_att)]
+    if kind == "attention":
+        idx.copy_(torch.sort(torch.randint(0, T, (B, Q, w.topk), device=dev), dim=-1).values)
+    for _ in range(args.warmup + args.steps):
+        if kind == "indexer":
+            dsa.indexer_scores(cfg, q_idx, wt, k_idx, q_pos, scores)
+        elif kind == "topk":
+            dsa.topk_select(cfg, scores, q_pos, idx, ws)
+        elif kind == "attention":
+            for layer in range(n_att):
+                dsa.sparse_mla_attn(cfg, q[layer], kv[min(layer, len(kv) - 1)], idx, outs[layer], None, ws)
+        else:
+            dsa.indexshare_group_forward(cfg, q_idx, wt, k_idx, q_pos, q, kv, outs, idx, ws)
+    torch.cuda.synchronize()
+    status = dsa.get_device_error()
+    print(json.dumps({"profile_kernel": kind, "workload": w.name, "B": B, "Q": Q, "T": T,
+                      "launches": args.warmup + args.steps, "device_error": status}))
+    if status != 0:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -521,11 +580,22 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variant", action="store_true", help="skip the per-layer-indexer comparison")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--settle", type=float, default=1.0, help="seconds of untimed load before timing (clock record)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None, help="smaller batch (a small case for profiling)")
+    ap.add_argument("--profile-kernel", choices=["indexer", "topk", "attention", "group"], default=None,
+                    help="only run one entry point a few times (for ncu captures) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     w = wl.WORKLOADS[args.workload]
+    if args.batch is not None:
+        import dataclasses
+        w = dataclasses.replace(w, B=args.batch)
     world, rank, local = dist_env()
+    if args.profile_kernel:
+        profile_kernel(args, w)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, w)), flush=True)
