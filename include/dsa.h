@@ -144,6 +144,29 @@ dsa_status_t dsa_mtp_draft_attn(const dsa_config_t *cfg, const int32_t *idx0,
                                 const dsa_bf16_t *q_steps, const dsa_bf16_t *kv, int S, int B, int T,
                                 dsa_bf16_t *out, void *ws, size_t ws_bytes, dsa_stream_t stream);
 
+/* Sparse MLA attention without any caller workspace (same arguments and
+ * result as dsa_sparse_mla_attn, minus ws/ws_bytes).  The pages have no
+ * counterpart: this is for callers that cannot allocate device memory at the
+ * point of the call -- e.g. code running where cudaMalloc is forbidden or
+ * unsafe (inside a framework's memory pool or an allocator callback, or a
+ * host that reserved all device memory up front) -- and so cannot provide
+ * the split-k scratch that dsa_sparse_mla_attn takes from its workspace.
+ * The scratch is instead a fixed 16 MiB array compiled into the library,
+ * which every GPU that loads the library keeps until the process exits.
+ *   - At most 64 query rows (B * Q <= 64) per call; larger calls return
+ *     DSA_ERR_WORKSPACE before anything is enqueued.  The key range is split
+ *     over fewer blocks than dsa_sparse_mla_attn may use when the rows'
+ *     partial results would not fit, so outputs agree with it to rounding.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array and nothing in it needs to
+ *     start at zero; calls whose work overlaps on the GPU (different streams,
+ *     no ordering between them) race on it and must not be issued.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+dsa_status_t dsa_sparse_mla_attn_noalloc(const dsa_config_t *cfg, const dsa_bf16_t *q, const dsa_bf16_t *kv,
+                                         const int32_t *idx, int B, int Q, int T, dsa_bf16_t *out, float *lse,
+                                         dsa_stream_t stream);
+
 /* Human-readable name of a status. */
 const char *dsa_status_string(dsa_status_t status);
 

@@ -22,7 +22,7 @@ STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "D
 # every symbol include/dsa.h declares
 EXPORTS = ("dsa_config_default", "dsa_workspace_bytes", "dsa_indexer_scores", "dsa_topk_select",
            "dsa_sparse_mla_attn", "dsa_indexshare_group_forward", "dsa_mtp_draft_attn",
-           "dsa_status_string", "dsa_get_device_error")
+           "dsa_status_string", "dsa_get_device_error", "dsa_sparse_mla_attn_noalloc")
 
 
 class DsaConfig(ctypes.Structure):
@@ -60,8 +60,10 @@ def lib() -> ctypes.CDLL:
                                                    ctypes.POINTER(_VP), _I, _I, _I, _I, ctypes.POINTER(_VP),
                                                    _VP, _VP, _SZ, _VP]
         L.dsa_mtp_draft_attn.argtypes = [_CFG, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _SZ, _VP]
+        L.dsa_sparse_mla_attn_noalloc.argtypes = [_CFG, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP]
         for name in ("dsa_indexer_scores", "dsa_topk_select", "dsa_sparse_mla_attn",
-                     "dsa_indexshare_group_forward", "dsa_mtp_draft_attn", "dsa_get_device_error"):
+                     "dsa_indexshare_group_forward", "dsa_mtp_draft_attn", "dsa_get_device_error",
+                     "dsa_sparse_mla_attn_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         L.dsa_get_device_error.argtypes = [_VP]
         L.dsa_status_string.argtypes = [ctypes.c_int]
@@ -138,6 +140,20 @@ def sparse_mla_attn(cfg, q, kv, idx, out, lse=None, ws=None, stream=None):
     B, Q, T = q.shape[0], q.shape[1], kv.shape[1]
     _check(lib().dsa_sparse_mla_attn(ctypes.byref(cfg), _p(q), _p(kv), _p(idx), B, Q, T, _p(out), _p(lse),
                                      _p(ws), 0 if ws is None else ws.numel(), _s(stream)), "dsa_sparse_mla_attn")
+
+
+def sparse_mla_attn_noalloc(cfg, q, kv, idx, out, lse=None, stream=None):
+    """Same as sparse_mla_attn, for callers that cannot allocate device memory:
+    no workspace argument; the library's own fixed 16 MiB scratch is used
+    instead.  At most 64 query rows (B * Q) per call; calls that run at the same
+    time on one GPU share that scratch and must not overlap."""
+    _need(q, "q", torch.bfloat16, 4); _need(kv, "kv", torch.bfloat16, 3); _need(idx, "idx", torch.int32, 3)
+    _need(out, "out", torch.bfloat16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    B, Q, T = q.shape[0], q.shape[1], kv.shape[1]
+    _check(lib().dsa_sparse_mla_attn_noalloc(ctypes.byref(cfg), _p(q), _p(kv), _p(idx), B, Q, T, _p(out), _p(lse),
+                                             _s(stream)), "dsa_sparse_mla_attn_noalloc")
 
 
 def indexshare_group_forward(cfg, q_idx, w, k_idx, q_pos, qs: Sequence[torch.Tensor], kvs: Sequence[torch.Tensor],

@@ -421,6 +421,93 @@ dsa_status_t dsa_mtp_draft_attn(const dsa_config_t *cfg, const int32_t *idx0, co
                           cfg->sm_scale, reinterpret_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Attention without a caller workspace: the split-k partials live in a fixed
+// array compiled into the library.  In host code `g_noalloc_partials` names a
+// host-side stand-in, not device memory: its device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+constexpr int kNoAllocMaxRows = 64;                          // B * Q per call
+constexpr size_t kPartialTileBytes = size_t(kHeads) * kLora * 4;  // one (row, split) partial O
+constexpr size_t kPartialMlBytes = size_t(kHeads) * 2 * 4;        // its (max, sum) per head
+constexpr int kNoAllocTiles = static_cast<int>(kNoAllocScratchBytes / (kPartialTileBytes + kPartialMlBytes));
+
+static __device__ __align__(256) unsigned char g_noalloc_partials[kNoAllocScratchBytes];
+
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the static scratch on the current device (looked up once).
+bool noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_partials) != cudaSuccess || ptr == nullptr) return false;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+dsa_status_t dsa_sparse_mla_attn_noalloc(const dsa_config_t *cfg, const dsa_bf16_t *q, const dsa_bf16_t *kv,
+                                         const int32_t *idx, int B, int Q, int T, dsa_bf16_t *out, float *lse,
+                                         dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  DSA_TRY(check_sizes(B, Q, T));
+  if (!q || !kv || !idx || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(idx) || !aligned16(out) || (lse && !aligned16(lse)))
+    return DSA_ERR_ALIGNMENT;
+  const int rows = B * Q;
+  if (rows > kNoAllocMaxRows) return DSA_ERR_WORKSPACE;  // beyond what the static scratch holds
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  void *scratch = nullptr;
+  if (!noalloc_scratch(&scratch)) return DSA_ERR_CUDA;
+  // the usual split of the index slots, with no more (row, split) partials
+  // than the array holds; rows <= 64 always leaves at least one split
+  AttnShape a = attn_shape(rows, cfg->topk, dev->sms);
+  const int max_splits = kNoAllocTiles / rows;
+  if (a.nsplit > max_splits) {
+    const int nblocks = (cfg->topk + dsa::attn::kBlk - 1) / dsa::attn::kBlk;
+    a.bps = (nblocks + max_splits - 1) / max_splits;
+    a.nsplit = (nblocks + a.bps - 1) / a.bps;
+  }
+  dsa::attn::Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.q[0] = reinterpret_cast<const __nv_bfloat16 *>(q);
+  p.kv[0] = reinterpret_cast<const __nv_bfloat16 *>(kv);
+  p.out[0] = reinterpret_cast<__nv_bfloat16 *>(out);
+  p.lse[0] = lse;
+  p.idx = idx;
+  p.n_layers = 1;
+  p.Q = Q;
+  p.T = T;
+  p.K = cfg->topk;
+  p.rows = rows;
+  p.nsplit = a.nsplit;
+  p.blocks_per_split = a.bps;
+  // every (row, split) partial is fully written before the combine reads it,
+  // so nothing in the array has to be cleared between calls
+  p.part_o = static_cast<float *>(scratch);
+  p.part_ml = reinterpret_cast<float *>(static_cast<unsigned char *>(scratch) + kNoAllocTiles * kPartialTileBytes);
+  p.scale_log2 = cfg->sm_scale * 1.4426950408889634f;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  dsa::attn::sparse_mla_kernel<<<static_cast<unsigned>(p.nsplit * rows), dsa::attn::kThreads, dsa::attn::kSmemBytes,
+                                 st>>>(p);
+  if (p.nsplit > 1) dsa::attn::combine_kernel<<<dim3(kHeads, rows), 128, 0, st>>>(p);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
 const char *dsa_status_string(dsa_status_t s) {
   switch (s) {
     case DSA_OK: return "DSA_OK";
