@@ -50,6 +50,10 @@ bool device_state(DeviceState **out) {
                                dsa::indexer::Cfg<4>::kSmemBytes) == cudaSuccess;
     ok &= cudaFuncSetAttribute(dsa::attn::sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dsa::attn::kSmemBytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::topk::topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::topk::kSelectSmem) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::topk::topk_chunk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::topk::kSelectSmem) == cudaSuccess;
     if (!ok) return false;
     if (g_encode == nullptr) {
       void *fn = nullptr;
@@ -140,7 +144,7 @@ AttnShape attn_shape(long long rowsL, int K, int sms) {
 }
 
 struct Layout {
-  size_t scores = 0, ghist = 0, counts = 0, idx = 0, part_o = 0, part_ml = 0, total = 0;
+  size_t scores = 0, ghist = 0, gcount = 0, cand = 0, idx = 0, part_o = 0, part_ml = 0, total = 0;
   TopkShape ts;
 };
 
@@ -161,10 +165,14 @@ Layout layout(int B, int Q, int T, int n_layers, int K, int sms) {
   size_t off = 0;
   L.scores = off;
   off = align_up(off + static_cast<size_t>(rows) * T * sizeof(float), 256);
+  // chunked top-k: digit histograms and candidate counters (zeroed by one
+  // memset, so they are adjacent), then room for T candidates per row
   L.ghist = off;
-  if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(dsa::topk::kPasses) * rows * dsa::topk::kMaxBins * 4, 256);
-  L.counts = off;
-  if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(rows) * L.ts.nchunk * 2 * 4, 256);
+  if (L.ts.nchunk > 1) off += static_cast<size_t>(rows) * 2 * dsa::topk::kBins * 4;
+  L.gcount = off;
+  if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(rows) * 4, 256);
+  L.cand = off;
+  if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(rows) * T * 8, 256);
   L.idx = off;
   off = align_up(off + static_cast<size_t>(rows) * K * sizeof(int32_t), 256);
   // partials: the largest need over a single-layer call and an n_layers call
@@ -182,8 +190,11 @@ Layout layout(int B, int Q, int T, int n_layers, int K, int sms) {
 // ---------------------------------------------------------------------------
 // Launch helpers (arguments already validated)
 // ---------------------------------------------------------------------------
+// ghist: when non-null (and Q == 1), the indexer also counts the top-k's
+// digit-0 histograms into it (which must be zeroed before).
 dsa_status_t launch_indexer(const DeviceState &dev, const dsa_bf16_t *q_idx, const float *w, const dsa_bf16_t *k_idx,
-                            const int32_t *q_pos, int B, int Q, int T, float *scores, cudaStream_t stream) {
+                            const int32_t *q_pos, int B, int Q, int T, float *scores, cudaStream_t stream,
+                            uint32_t *ghist = nullptr) {
   const int QG = Q == 1 ? 1 : (Q == 2 ? 2 : 4);
   CUtensorMap tk, tq;
   if (!make_tmap_128(&tk, k_idx, static_cast<unsigned long long>(B) * T, dsa::indexer::kTileKeys)) return DSA_ERR_CUDA;
@@ -200,6 +211,7 @@ dsa_status_t launch_indexer(const DeviceState &dev, const dsa_bf16_t *q_idx, con
   p.ntiles = (T + dsa::indexer::kTileKeys - 1) / dsa::indexer::kTileKeys;
   p.units = static_cast<long long>(B) * p.ngroups * p.ntiles;
   p.stream_keys = p.ngroups == 1 ? 1 : 0;
+  p.ghist = QG == 1 ? ghist : nullptr;
   const long long grid = p.units < dev.sms ? p.units : dev.sms;
   if (QG == 1)
     dsa::indexer::indexer_scores_kernel<1><<<static_cast<unsigned>(grid), dsa::indexer::kThreads,
@@ -213,11 +225,19 @@ dsa_status_t launch_indexer(const DeviceState &dev, const dsa_bf16_t *q_idx, con
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
+// Clears the chunked top-k's histograms and counters (before the indexer when
+// it counts the digit-0 histogram itself).
+dsa_status_t clear_topk_state(const Layout &L, uint8_t *ws, cudaStream_t stream) {
+  if (L.ts.nchunk <= 1) return DSA_OK;
+  return cudaMemsetAsync(ws + L.ghist, 0, L.cand - L.ghist, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+// hist_done: the digit-0 histograms were already counted (by the indexer).
 dsa_status_t launch_topk(const Layout &L, uint8_t *ws, const float *scores, const int32_t *q_pos, int rows, int T,
-                         int K, int32_t *idx, cudaStream_t stream) {
+                         int K, int32_t *idx, cudaStream_t stream, bool hist_done = false) {
   using namespace dsa::topk;
   if (L.ts.nchunk == 1) {
-    topk_row_kernel<<<rows, kThreads, 0, stream>>>(scores, q_pos, T, K, idx);
+    topk_row_kernel<<<rows, kThreads, kSelectSmem, stream>>>(scores, q_pos, T, K, idx);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   }
   ChunkParams p;
@@ -229,16 +249,17 @@ dsa_status_t launch_topk(const Layout &L, uint8_t *ws, const float *scores, cons
   p.chunk = L.ts.chunk;
   p.nchunk = L.ts.nchunk;
   p.ghist = reinterpret_cast<uint32_t *>(ws + L.ghist);
-  p.counts = reinterpret_cast<uint32_t *>(ws + L.counts);
+  p.gcount = reinterpret_cast<uint32_t *>(ws + L.gcount);
+  p.cand = reinterpret_cast<uint64_t *>(ws + L.cand);
   p.idx = idx;
-  if (cudaMemsetAsync(p.ghist, 0, static_cast<size_t>(kPasses) * rows * kMaxBins * 4, stream) != cudaSuccess)
-    return DSA_ERR_CUDA;
   const dim3 grid(p.nchunk, rows);
-  topk_chunk_hist_kernel<0><<<grid, kThreads, 0, stream>>>(p);
-  topk_chunk_hist_kernel<1><<<grid, kThreads, 0, stream>>>(p);
-  topk_chunk_hist_kernel<2><<<grid, kThreads, 0, stream>>>(p);
-  topk_chunk_count_kernel<<<grid, kThreads, 0, stream>>>(p);
-  topk_chunk_write_kernel<<<grid, kThreads, 0, stream>>>(p);
+  if (!hist_done) {
+    if (clear_topk_state(L, ws, stream) != DSA_OK) return DSA_ERR_CUDA;
+    topk_chunk_hist_kernel<<<grid, kThreads, 0, stream>>>(p);
+  }
+  topk_chunk_scan_kernel<1><<<grid, kThreads, 0, stream>>>(p);
+  topk_chunk_scan_kernel<2><<<grid, kThreads, 0, stream>>>(p);
+  topk_chunk_select_kernel<<<rows, kThreads, kSelectSmem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -384,8 +405,11 @@ dsa_status_t dsa_indexshare_group_forward(const dsa_config_t *cfg, const dsa_bf1
   float *scores = reinterpret_cast<float *>(wsb + L.scores);
   int32_t *idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(wsb + L.idx);
   // IndexShare: the indexer and top-k run once for the whole group ...
-  DSA_TRY(launch_indexer(*dev, q_idx, w, k_idx, q_pos, B, Q, T, scores, st));
-  DSA_TRY(launch_topk(L, wsb, scores, q_pos, B * Q, T, cfg->topk, idx, st));
+  const bool fuse_hist = Q == 1 && L.ts.nchunk > 1;
+  if (fuse_hist) DSA_TRY(clear_topk_state(L, wsb, st));
+  DSA_TRY(launch_indexer(*dev, q_idx, w, k_idx, q_pos, B, Q, T, scores, st,
+                         fuse_hist ? reinterpret_cast<uint32_t *>(wsb + L.ghist) : nullptr));
+  DSA_TRY(launch_topk(L, wsb, scores, q_pos, B * Q, T, cfg->topk, idx, st, fuse_hist));
   // ... and every layer of the group attends over the same index set.
   return launch_attention(*dev, L, wsb, q, kv, out, nullptr, n_layers, idx, B * Q, Q, T, cfg->topk, cfg->sm_scale,
                           st);

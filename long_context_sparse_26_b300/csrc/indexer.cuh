@@ -18,6 +18,12 @@
 //              head sum, one coalesced fp32 store per key and query.
 // Key tiles entirely after every query's position in the group are not
 // loaded; the epilogue writes -inf there.
+//
+// With one query per sequence (decode), the epilogue can also count each
+// visible score's top 11 key bits into a per-row histogram (the first step of
+// the top-k selection): each epilogue warp keeps its own shared-memory
+// histogram and adds it to the global one when its sequence changes, so the
+// count costs no extra pass over the scores and no cross-warp wait.
 #pragma once
 
 #include "common.cuh"
@@ -37,11 +43,13 @@ struct Cfg {
   static constexpr int N = QG * kHeads;                 // UMMA N: 64, 128 or 256
   static constexpr int kHalfBBytes = N * 64 * 2;
   static constexpr int kBBytes = 2 * kHalfBBytes;
-  static constexpr int kStages = QG == 1 ? 6 : (QG == 2 ? 5 : 4);
+  static constexpr int kStages = QG == 1 ? 5 : (QG == 2 ? 5 : 4);
+  static constexpr int kHistBytes = QG == 1 ? 4 * 2048 * 4 : 0;  // per-epilogue-warp digit-0 histograms
   static constexpr int kAcc = QG == 4 ? 2 : 4;          // accumulator buffers in TMEM
   static constexpr int kTmemCols = (kAcc * N <= 256) ? 256 : 512;
   static constexpr int kSmall = 1024 + 4 * QG * kHeads * 4;  // barriers + flags, then per-warp weights
-  static constexpr int kSmemBytes = 1024 + kStages * kABytes + kBBytes + kSmall;
+  static constexpr int kSmemBytes = 1024 + kStages * kABytes + kBBytes + kSmall + kHistBytes;
+  static_assert(kSmemBytes <= 232448, "shared memory per block");
   static_assert(kAcc * N <= kTmemCols, "accumulators must fit the allocation");
 };
 
@@ -54,7 +62,24 @@ struct Params {
   int ntiles;            // ceil(T / 128)
   long long units;       // B * ngroups * ntiles
   int stream_keys;       // 1: every key tile is read once (evict-first in L2)
+  uint32_t *ghist;       // QG == 1 only, may be null: [B][2][2048] digit-0 histograms (first half of each row)
 };
+
+constexpr int kHistBins = 2048;
+constexpr int kHistShift = 21;
+
+// Adds a warp's shared histogram to row `row` of the global one and clears it.
+__device__ __forceinline__ void flush_hist(uint32_t *whist, uint32_t *ghist, int row, int lane) {
+  uint32_t *g = ghist + (size_t)row * 2 * kHistBins;
+  for (int i = lane; i < kHistBins; i += 32) {
+    const uint32_t c = whist[i];
+    if (c) {
+      atomicAdd(g + i, c);
+      whist[i] = 0;
+    }
+  }
+  __syncwarp();
+}
 
 // Largest visible position of a query group (-1 if none), clamped to [-1, T-1].
 template <int QG>
@@ -93,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // [4 epilogue warps][QG][64]: each epilogue warp keeps its own copy of the
   // current group's head weights, so the warps never wait on one another.
   float *sw_all = reinterpret_cast<float *>(small + 1024);
+  uint32_t *hist_all = reinterpret_cast<uint32_t *>(small + C::kSmall);  // QG == 1: [4 warps][2048]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -228,6 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;                  // TMEM lanes this warp may read
     float *sw = sw_all + (warp - 2) * QG * kHeads;
+    uint32_t *whist = hist_all + (warp - 2) * kHistBins;
+    const bool do_hist = QG == 1 && p.ghist != nullptr;
+    if (do_hist) {
+      for (int i = lane; i < kHistBins; i += 32) whist[i] = 0;
+      __syncwarp();
+    }
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -240,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long seg = u / p.ntiles;
       const int tile = static_cast<int>(u - seg * p.ntiles);
       if (seg != cur_seg) {
+        if (do_hist && cur_seg >= 0) flush_hist(whist, p.ghist, b, lane);
         b = static_cast<int>(seg / p.ngroups);
         q0 = static_cast<int>(seg - (long long)b * p.ngroups) * QG;
         seg_max = group_max_pos<QG>(p, b, q0);
@@ -294,7 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (key < p.T) {
           float *row = p.scores + ((size_t)b * p.Q + q0 + i) * (size_t)p.T;
-          row[key] = (real && key <= posv[i]) ? s : -INFINITY;
+          const bool vis = real && key <= posv[i];
+          row[key] = vis ? s : -INFINITY;
+          if (do_hist && vis) atomicAdd(&whist[score_key(s) >> kHistShift], 1u);
         }
       }
       if (real) {
@@ -307,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (do_hist && cur_seg >= 0) flush_hist(whist, p.ghist, b, lane);
   }
 
   tc_fence_before();

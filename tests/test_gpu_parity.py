@@ -101,6 +101,7 @@ def _topk_case(scores_np, pos_np, k):
     (1, 2, 50_000, 2048, "equal"),       # every score equal: pure tie-break
     (1, 320, 5000, 2048, "normal"),      # many rows: one block per row
     (1, 320, 3000, 700, "ints"),
+    (1, 300, 13000, 2048, "equal"),      # many rows, candidates overflow shared memory: fallback passes
     (4, 1, 9000, 7, "normal"),           # tiny k
     (2, 2, 1500, 2048, "normal"),        # L < k: -1 padding
 ])
@@ -257,6 +258,29 @@ def test_group_equals_four_independent_layers():
     dsa.topk_select(cfg, scores, inp.q_pos, idx2, ws1)
     torch.cuda.synchronize()
     assert torch.equal(idx, idx2)
+
+
+@pytest.mark.parametrize("B,T,dup", [(3, 50_000, False), (2, 120_000, True), (5, 9_000, True)])
+def test_group_decode_topk_bit_exact(B, T, dup):
+    """One query per sequence over a long context: the group's index set (whose
+    first histogram is counted inside the indexer) equals the oracle's top-k of
+    the very same fp32 scores, bit for bit, including exact ties made by
+    duplicated keys."""
+    cfg = dsa.default_config()
+    q_idx, w, k_idx, pos = _indexer_inputs(B, 1, T, T - 1, seed=T + B)
+    if dup:   # copy a block of keys elsewhere: identical scores at different positions
+        k_idx[:, T // 2:T // 2 + 3000] = k_idx[:, 1000:4000]
+        k_idx[:, T - 500:] = k_idx[:, 200:700]
+    q = [wl.mla_queries(B, 1, 5, layer, DEV) for layer in range(4)]
+    kv = [wl.latent_cache(B, T, 5, layer, DEV) for layer in range(4)]
+    outs = [torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=DEV) for _ in range(4)]
+    idx = torch.empty(B, 1, 2048, dtype=torch.int32, device=DEV)
+    dsa.indexshare_group_forward(cfg, q_idx, w, k_idx, pos, q, kv, outs, idx, dsa.alloc_workspace(cfg, B, 1, T, 4))
+    scores = torch.empty(B, 1, T, device=DEV)
+    dsa.indexer_scores(cfg, q_idx, w, k_idx, pos, scores)
+    torch.cuda.synchronize()
+    ora = oracle.topk_select(scores.cpu().double().numpy(), pos.cpu().numpy(), 2048)
+    assert np.array_equal(idx.cpu().numpy(), ora)
 
 
 def test_group_is_deterministic():
