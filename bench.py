@@ -458,18 +458,21 @@ def run_e2e(args, w, cfg, inp, outs, idx, scores, ws, stream, dsa) -> dict:
 
 def run_per_layer_variant(args, w, cfg, inp, dev, group_ms, dsa) -> dict:
     """Without IndexShare: each of the 4 layers runs its own indexer + top-k."""
-    per = wl.make_inputs(w, dev, per_layer_indexers=True)
+    idx_q, idx_w, idx_k = wl.per_layer_indexers_of(w, inp.q_idx, inp.w, inp.k_idx, dev)
     B, Q, T = w.B, w.Q, w.T
     stream = torch.cuda.Stream(device=dev)
     ws = dsa.alloc_workspace(cfg, B, Q, T, 1, dev)
     scores = torch.empty(B, Q, T, device=dev)
     idxs = [torch.empty(B, Q, w.topk, dtype=torch.int32, device=dev) for _ in range(w.n_layers)]
     outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(w.n_layers)]
+    # the inputs were drawn on the default stream and the buffers above may reuse
+    # memory that its pending kernels still write: finish them before `stream` runs
+    torch.cuda.synchronize()
 
     def step():
         for layer in range(w.n_layers):
-            dsa.indexer_scores(cfg, per.idx_q[layer], per.idx_w[layer], per.idx_k[layer], per.q_pos, scores, stream)
-            dsa.topk_select(cfg, scores, per.q_pos, idxs[layer], ws, stream)
+            dsa.indexer_scores(cfg, idx_q[layer], idx_w[layer], idx_k[layer], inp.q_pos, scores, stream)
+            dsa.topk_select(cfg, scores, inp.q_pos, idxs[layer], ws, stream)
             dsa.sparse_mla_attn(cfg, inp.q[layer], inp.kv[layer], idxs[layer], outs[layer], None, ws, stream)
 
     with torch.cuda.stream(stream):
@@ -489,7 +492,7 @@ def run_per_layer_variant(args, w, cfg, inp, dev, group_ms, dsa) -> dict:
     stream.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     alg = w.n_layers * B * T * wl.IDX_DIM * 2 + w.n_layers * B * Q * w.topk * wl.D_QK * 2
-    del per
+    del idx_q, idx_w, idx_k
     torch.cuda.empty_cache()
     return {"ms_per_step": ms, "tokens_per_s": B * Q / (ms / 1e3), "algorithmic_bytes": alg,
             "indexshare_speedup": ms / group_ms,
@@ -592,13 +595,15 @@ def main():
     if args.batch is not None:
         import dataclasses
         w = dataclasses.replace(w, B=args.batch)
+    if args.impl == "reference":
+        # the oracle is a host program: rank 0 alone runs and prints it, the
+        # other ranks exit without work (no process group is needed)
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return
     world, rank, local = dist_env()
     if args.profile_kernel:
         profile_kernel(args, w)
-        return
-    if args.impl == "reference":
-        if rank == 0:
-            print(json.dumps(run_reference(args, w)), flush=True)
         return
     res = run_ours(args, w, world, rank, local)
     if rank == 0 and res is not None:

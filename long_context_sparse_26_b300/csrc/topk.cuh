@@ -452,7 +452,11 @@ __global__ void __launch_bounds__(kThreads) topk_chunk_select_kernel(const Chunk
   const int L = visible_length(p.q_pos, row, p.T);
   int32_t *out = p.idx + (size_t)row * p.K;
   if (write_short_row(L, p.K, out)) return;
-  const uint32_t n = p.gcount[row];  // <= L: every candidate was stored
+  uint32_t n = p.gcount[row];  // <= L: each visible position is appended at most once
+  if (n > static_cast<uint32_t>(L)) {  // a corrupted counter: report it, never read past the row
+    if (threadIdx.x == 0) raise_error(kErrDeviceCheck);
+    n = static_cast<uint32_t>(L);
+  }
   const uint64_t *gc = p.cand + (size_t)row * p.T;
   const uint64_t *src = gc;
   if (n <= static_cast<uint32_t>(kSmemCand)) {

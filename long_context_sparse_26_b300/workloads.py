@@ -194,10 +194,19 @@ def make_inputs(wl: Workload, device="cpu", per_layer_indexers: bool = False,
     q_steps = draft_queries(wl.mtp_steps, B, wl.seed, device) if wl.kind == "mtp" else None
     inp = Inputs(q_idx, w, k_idx, q_pos, qs, kvs, q_steps)
     if per_layer_indexers:
-        inp.idx_q, inp.idx_w, inp.idx_k = [q_idx], [w], [k_idx]
-        for layer in range(1, wl.n_layers):
-            s = wl.seed + 17 * layer
-            inp.idx_q.append(indexer_queries(B, wl.Q, s, device))
-            inp.idx_w.append(head_weights(B, wl.Q, s, device))
-            inp.idx_k.append(indexer_keys(B, T, s, device))
+        inp.idx_q, inp.idx_w, inp.idx_k = per_layer_indexers_of(wl, q_idx, w, k_idx, device)
     return inp
+
+
+def per_layer_indexers_of(wl: Workload, q_idx: torch.Tensor, w: torch.Tensor, k_idx: torch.Tensor,
+                          device="cpu"):
+    """Indexer inputs of every layer when each layer has its own indexer (no
+    IndexShare): layer 0 keeps the given ones, layers 1.. draw their own."""
+    B, Q, T = q_idx.shape[0], q_idx.shape[1], k_idx.shape[1]
+    qs, ws, ks = [q_idx], [w], [k_idx]
+    for layer in range(1, wl.n_layers):
+        s = wl.seed + 17 * layer
+        qs.append(indexer_queries(B, Q, s, device))
+        ws.append(head_weights(B, Q, s, device))
+        ks.append(indexer_keys(B, T, s, device))
+    return qs, ws, ks
