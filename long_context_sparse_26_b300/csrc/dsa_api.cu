@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "indexer.cuh"
 #include "sparse_mla.cuh"
+#include "sparse_mla_tc.cuh"
 #include "topk.cuh"
 
 namespace {
@@ -48,8 +49,8 @@ bool device_state(DeviceState **out) {
                                dsa::indexer::Cfg<2>::kSmemBytes) == cudaSuccess;
     ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dsa::indexer::Cfg<4>::kSmemBytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(dsa::attn::sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dsa::attn::kSmemBytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::mla::sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::mla::kSmemBytes) == cudaSuccess;
     ok &= cudaFuncSetAttribute(dsa::topk::topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dsa::topk::kSelectSmem) == cudaSuccess;
     ok &= cudaFuncSetAttribute(dsa::topk::topk_chunk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -75,6 +76,19 @@ bool device_state(DeviceState **out) {
 bool make_tmap_128(CUtensorMap *map, const void *ptr, unsigned long long rows, unsigned box_rows) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(kIdxDim * 2)};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 2D bf16 tensor map over a row-major [rows, 576] matrix (the query heads of
+// an attention call), 128-byte swizzle, box = 64 columns x box_rows rows.
+bool make_tmap_576(CUtensorMap *map, const void *ptr, unsigned long long rows, unsigned box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kLora + kRope), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>((kLora + kRope) * 2)};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
@@ -130,17 +144,25 @@ struct AttnShape {
   int nsplit = 1, bps = 1;
 };
 
+// Splits of each row's index slots over blocks (one block per SM at a time):
+// the fewest waves x tiles per block, where a split also costs its fp32
+// partial (written, then read by the combine: about 7 tiles' worth of bytes).
 AttnShape attn_shape(long long rowsL, int K, int sms) {
-  AttnShape a;
-  const int nblocks = (K + dsa::attn::kBlk - 1) / dsa::attn::kBlk;
-  int ns = 1;
-  if (rowsL < 2LL * sms) ns = static_cast<int>((2LL * sms + rowsL - 1) / rowsL);
-  ns = ns > nblocks ? nblocks : ns;
-  ns = ns > 16 ? 16 : ns;
-  ns = ns < 1 ? 1 : ns;
-  a.bps = (nblocks + ns - 1) / ns;
-  a.nsplit = (nblocks + a.bps - 1) / a.bps;
-  return a;
+  AttnShape best;
+  const int nblocks = (K + dsa::mla::kKeys - 1) / dsa::mla::kKeys;
+  long long best_cost = -1;
+  for (int ns = 1; ns <= 16 && ns <= nblocks; ++ns) {
+    const int bps = (nblocks + ns - 1) / ns;
+    const int nsr = (nblocks + bps - 1) / bps;
+    const long long waves = (rowsL * nsr + sms - 1) / sms;
+    const long long cost = waves * (bps + (nsr > 1 ? 7 : 0));
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best.nsplit = nsr;
+      best.bps = bps;
+    }
+  }
+  return best;
 }
 
 struct Layout {
@@ -214,13 +236,13 @@ dsa_status_t launch_indexer(const DeviceState &dev, const dsa_bf16_t *q_idx, con
   p.ghist = QG == 1 ? ghist : nullptr;
   const long long grid = p.units < dev.sms ? p.units : dev.sms;
   if (QG == 1)
-    dsa::indexer::indexer_scores_kernel<1><<<static_cast<unsigned>(grid), dsa::indexer::kThreads,
+    dsa::indexer::indexer_scores_kernel<1><<<static_cast<unsigned>(grid), dsa::indexer::Cfg<1>::kThreads,
                                               dsa::indexer::Cfg<1>::kSmemBytes, stream>>>(tk, tq, p);
   else if (QG == 2)
-    dsa::indexer::indexer_scores_kernel<2><<<static_cast<unsigned>(grid), dsa::indexer::kThreads,
+    dsa::indexer::indexer_scores_kernel<2><<<static_cast<unsigned>(grid), dsa::indexer::Cfg<2>::kThreads,
                                               dsa::indexer::Cfg<2>::kSmemBytes, stream>>>(tk, tq, p);
   else
-    dsa::indexer::indexer_scores_kernel<4><<<static_cast<unsigned>(grid), dsa::indexer::kThreads,
+    dsa::indexer::indexer_scores_kernel<4><<<static_cast<unsigned>(grid), dsa::indexer::Cfg<4>::kThreads,
                                               dsa::indexer::Cfg<4>::kSmemBytes, stream>>>(tk, tq, p);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
@@ -263,6 +285,27 @@ dsa_status_t launch_topk(const Layout &L, uint8_t *ws, const float *scores, cons
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
+// Enqueues the tensor-core attention kernel (and the split combine) for
+// filled-in Params over B sequences; encodes each layer's tensor maps.
+dsa_status_t enqueue_attention(const dsa::attn::Params &p, int B, cudaStream_t stream) {
+  (void)B;
+  dsa::mla::Maps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  for (int l = 0; l < p.n_layers; ++l)
+    if (!make_tmap_576(&maps.q[l], p.q[l], static_cast<unsigned long long>(p.rows) * kHeads, kHeads))
+      return DSA_ERR_CUDA;
+  const long long blocks = static_cast<long long>(p.n_layers) * p.nsplit * p.rows;
+  dsa::mla::sparse_mla_tc_kernel<<<static_cast<unsigned>(blocks), dsa::mla::kThreads, dsa::mla::kSmemBytes, stream>>>(
+      maps, p);
+  if (p.nsplit > 1) {
+    const dim3 cgrid(kHeads, static_cast<unsigned>(static_cast<long long>(p.rows) * p.n_layers));
+    dsa::attn::combine_kernel<<<cgrid, 128, 0, stream>>>(p);
+  }
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+inline int B_of(int rows, int Q) { return rows / Q; }
+
 // Attention over n_layers layers (or draft steps) that share one index set.
 dsa_status_t launch_attention(const DeviceState &dev, const Layout &L, uint8_t *ws, const dsa_bf16_t *const *q,
                               const dsa_bf16_t *const *kv, dsa_bf16_t *const *out, float *const *lse, int n_layers,
@@ -288,13 +331,7 @@ dsa_status_t launch_attention(const DeviceState &dev, const Layout &L, uint8_t *
   p.part_o = reinterpret_cast<float *>(ws + L.part_o);
   p.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
   p.scale_log2 = sm_scale * 1.4426950408889634f;
-  const long long blocks = static_cast<long long>(n_layers) * p.nsplit * rows;
-  dsa::attn::sparse_mla_kernel<<<static_cast<unsigned>(blocks), dsa::attn::kThreads, dsa::attn::kSmemBytes, stream>>>(p);
-  if (p.nsplit > 1) {
-    const dim3 cgrid(kHeads, static_cast<unsigned>(static_cast<long long>(rows) * n_layers));
-    dsa::attn::combine_kernel<<<cgrid, 128, 0, stream>>>(p);
-  }
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return enqueue_attention(p, B_of(rows, Q), stream);
 }
 
 #define DSA_TRY(expr)                 \
@@ -502,7 +539,7 @@ dsa_status_t dsa_sparse_mla_attn_noalloc(const dsa_config_t *cfg, const dsa_bf16
   AttnShape a = attn_shape(rows, cfg->topk, dev->sms);
   const int max_splits = kNoAllocTiles / rows;
   if (a.nsplit > max_splits) {
-    const int nblocks = (cfg->topk + dsa::attn::kBlk - 1) / dsa::attn::kBlk;
+    const int nblocks = (cfg->topk + dsa::mla::kKeys - 1) / dsa::mla::kKeys;
     a.bps = (nblocks + max_splits - 1) / max_splits;
     a.nsplit = (nblocks + a.bps - 1) / a.bps;
   }
@@ -525,11 +562,7 @@ dsa_status_t dsa_sparse_mla_attn_noalloc(const dsa_config_t *cfg, const dsa_bf16
   p.part_o = static_cast<float *>(scratch);
   p.part_ml = reinterpret_cast<float *>(static_cast<unsigned char *>(scratch) + kNoAllocTiles * kPartialTileBytes);
   p.scale_log2 = cfg->sm_scale * 1.4426950408889634f;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  dsa::attn::sparse_mla_kernel<<<static_cast<unsigned>(p.nsplit * rows), dsa::attn::kThreads, dsa::attn::kSmemBytes,
-                                 st>>>(p);
-  if (p.nsplit > 1) dsa::attn::combine_kernel<<<dim3(kHeads, rows), 128, 0, st>>>(p);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return enqueue_attention(p, B, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char *dsa_status_string(dsa_status_t s) {

@@ -9,13 +9,16 @@
 // memory with one key per TMEM lane, so the ReLU and the weighted head sum run
 // inside one thread: no shuffles, no shared-memory round trip.
 //
-// Warp roles (192 threads, one block per SM, persistent over a contiguous
-// range of (sequence, query group, key tile) units):
+// Warp roles (one block per SM, persistent over a contiguous range of
+// (sequence, query group, key tile) units):
 //   warp 0     TMA producer: key tiles (two 64-dim halves, 128-byte swizzle)
 //              into a ring of stages; the query-group operand once per group.
 //   warp 1     allocates tensor memory and issues tcgen05.mma (one thread).
-//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes, ReLU, weighted
-//              head sum, one coalesced fp32 store per key and query.
+//   warps 2..  epilogue: tcgen05.ld of their 32 TMEM lanes, ReLU, weighted
+//              head sum, one coalesced fp32 store per key and query.  Four
+//              warps (one per TMEM lane quarter) for 1 or 2 queries per
+//              group; eight for 4 queries (two per quarter, two queries each),
+//              so that every scheduler interleaves two epilogue warps.
 // Key tiles entirely after every query's position in the group are not
 // loaded; the epilogue writes -inf there.
 //
@@ -36,7 +39,6 @@ constexpr int kDim = 128;
 constexpr int kTileKeys = 128;                     // UMMA M
 constexpr int kHalfABytes = kTileKeys * 64 * 2;    // one 64-dim half of a key tile: 16 KB
 constexpr int kABytes = 2 * kHalfABytes;           // 32 KB per stage
-constexpr int kThreads = 192;
 
 template <int QG>
 struct Cfg {
@@ -44,6 +46,9 @@ struct Cfg {
   static constexpr int kHalfBBytes = N * 64 * 2;
   static constexpr int kBBytes = 2 * kHalfBBytes;
   static constexpr int kStages = QG == 1 ? 5 : (QG == 2 ? 5 : 4);
+  static constexpr int kEpiWarps = QG == 4 ? 8 : 4;
+  static constexpr int kQPW = QG * 4 / kEpiWarps;       // queries per epilogue warp
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kHistBytes = QG == 1 ? 4 * 2048 * 4 : 0;  // per-epilogue-warp digit-0 histograms
   static constexpr int kAcc = QG == 4 ? 2 : 4;          // accumulator buffers in TMEM
   static constexpr int kTmemCols = (kAcc * N <= 256) ? 256 : 512;
@@ -97,7 +102,7 @@ __device__ __forceinline__ int group_max_pos(const Params &p, int b, int q0) {
 }
 
 template <int QG>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
     indexer_scores_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                           const Params p) {
   using C = Cfg<QG>;
@@ -115,8 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *mma_done = bfree + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  // [4 epilogue warps][QG][64]: each epilogue warp keeps its own copy of the
-  // current group's head weights, so the warps never wait on one another.
+  // [epilogue warps][queries per warp][64]: each epilogue warp keeps its own
+  // copy of its queries' head weights, so the warps never wait on one another.
   float *sw_all = reinterpret_cast<float *>(small + 1024);
   uint32_t *hist_all = reinterpret_cast<uint32_t *>(small + C::kSmall);  // QG == 1: [4 warps][2048]
 
@@ -133,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < C::kAcc; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], C::kEpiWarps);
     }
     mbar_init(bfull, 1);
     mbar_init(bfree, 1);
@@ -252,9 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    constexpr int QPW = C::kQPW;
+    const int e = warp - 2;                        // epilogue warp index
     const int quarter = warp & 3;                  // TMEM lanes this warp may read
-    float *sw = sw_all + (warp - 2) * QG * kHeads;
-    uint32_t *whist = hist_all + (warp - 2) * kHistBins;
+    const int qb = (e >> 2) * QPW;                 // first query (within the group) of this warp
+    float *sw = sw_all + e * QPW * kHeads;
+    uint32_t *whist = hist_all + (e & 3) * kHistBins;
     const bool do_hist = QG == 1 && p.ghist != nullptr;
     if (do_hist) {
       for (int i = lane; i < kHistBins; i += 32) whist[i] = 0;
@@ -265,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     long long cur_seg = -1;
     int seg_max = -1;
-    int posv[QG];
+    int posv[QPW];
     int b = 0, q0 = 0;
     for (long long u = u_begin; u < u_end; ++u) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
@@ -277,15 +285,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         q0 = static_cast<int>(seg - (long long)b * p.ngroups) * QG;
         seg_max = group_max_pos<QG>(p, b, q0);
         __syncwarp();  // the warp is done with the previous group's weights
-        for (int i = lane; i < QG * kHeads; i += 32) {
-          const int q = q0 + i / kHeads;
+        for (int i = lane; i < QPW * kHeads; i += 32) {
+          const int q = q0 + qb + i / kHeads;
           sw[i] = q < p.Q ? __ldg(p.w + ((size_t)b * p.Q + q) * kHeads + (i % kHeads)) : 0.0f;
         }
 #pragma unroll
-        for (int i = 0; i < QG; ++i) {
-          int pos = (q0 + i < p.Q) ? __ldg(p.q_pos + (size_t)b * p.Q + q0 + i) : -1;
-          if (q0 + i < p.Q && (pos < 0 || pos >= p.T) && warp == 2 && lane == 0 && tile == 0)
-            raise_error(kErrDeviceCheck);
+        for (int i = 0; i < QPW; ++i) {
+          const int q = q0 + qb + i;
+          int pos = (q < p.Q) ? __ldg(p.q_pos + (size_t)b * p.Q + q) : -1;
+          if (q < p.Q && (pos < 0 || pos >= p.T) && lane == 0 && tile == 0) raise_error(kErrDeviceCheck);
           posv[i] = pos < 0 ? -1 : (pos >= p.T ? p.T - 1 : pos);
         }
         __syncwarp();
@@ -303,30 +311,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
 #pragma unroll
-      for (int i = 0; i < QG; ++i) {
-        if (q0 + i >= p.Q) break;
+      for (int i = 0; i < QPW; ++i) {
+        if (q0 + qb + i >= p.Q) break;
         float s = 0.0f;
         if (real) {
-          const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * C::N + i * kHeads);
+          // both 32-column halves of the query's 64 heads, one wait
+          const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * C::N + (qb + i) * kHeads);
           const float4 *w4 = reinterpret_cast<const float4 *>(sw + i * kHeads);
-          float v[32];
-          float s0 = 0.0f, s1 = 0.0f;
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32_nowait(taddr, v0);
+          tmem_ld_32x32b_x32_nowait(taddr + 32, v1);
+          tmem_wait_ld();
+          float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent chains
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tmem_ld_32x32b_x32(taddr + h * 32, v);
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              const float4 wv = w4[(h * 32 + j) >> 2];
-              s0 = fmaf(wv.x, fmaxf(v[j + 0], 0.0f), s0);
-              s1 = fmaf(wv.y, fmaxf(v[j + 1], 0.0f), s1);
-              s0 = fmaf(wv.z, fmaxf(v[j + 2], 0.0f), s0);
-              s1 = fmaf(wv.w, fmaxf(v[j + 3], 0.0f), s1);
-            }
+          for (int j = 0; j < 64; j += 4) {
+            const float4 wv = w4[j >> 2];
+            const uint32_t *v = j < 32 ? v0 + j : v1 + (j - 32);
+            const int c = (j >> 2) & 1;
+            a[4 * c + 0] = fmaf(wv.x, fmaxf(__uint_as_float(v[0]), 0.0f), a[4 * c + 0]);
+            a[4 * c + 1] = fmaf(wv.y, fmaxf(__uint_as_float(v[1]), 0.0f), a[4 * c + 1]);
+            a[4 * c + 2] = fmaf(wv.z, fmaxf(__uint_as_float(v[2]), 0.0f), a[4 * c + 2]);
+            a[4 * c + 3] = fmaf(wv.w, fmaxf(__uint_as_float(v[3]), 0.0f), a[4 * c + 3]);
           }
-          s = s0 + s1;
+          s = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
         }
         if (key < p.T) {
-          float *row = p.scores + ((size_t)b * p.Q + q0 + i) * (size_t)p.T;
+          float *row = p.scores + ((size_t)b * p.Q + q0 + qb + i) * (size_t)p.T;
           const bool vis = real && key <= posv[i];
           row[key] = vis ? s : -INFINITY;
           if (do_hist && vis) atomicAdd(&whist[score_key(s) >> kHistShift], 1u);

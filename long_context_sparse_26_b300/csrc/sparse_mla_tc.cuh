@@ -1,0 +1,538 @@
+// Sparse absorbed-MLA attention on the 5th-generation tensor cores.
+//
+// For one query token and one layer: z[h, j] = sm_scale * q[h, :] . kv[idx[j], :]
+// over 576-dim cached rows (512 compressed-KV dims, then 64 rotated RoPE dims),
+// p = softmax_j(z), O[h, :] = sum_j p[h, j] * kv[idx[j], :512]: the value is the
+// leading kv_lora_rank dims of the same row ("GLM-5.2 Explained: 1M Token
+// Context AI Agent Model", §2.1: K/V are loaded only for the selected
+// positions; §1.1: MLA is kept; kv_lora_rank = 512 in the GLM-5.2 config of
+// "GLM-5.2核心技术解析：IndexShare架构与MTP层优化详解"; 64 heads).
+//
+// Block = (layer, split, query row): it walks kKeys-key windows of its slice
+// of the index set.  Per window:
+//   gather  the selected latent rows in 32-row stages, 16-byte cp.async copies
+//           from the producer warps (a warp keeps only so many copies in
+//           flight, so the gather rate grows with the issuing warps; TMA
+//           gather4 copies of 4 x 128 B would be limited by their issue rate
+//           instead), into a ring of nine 64-dim panels x 128 rows x 128 B in
+//           the 128-byte-swizzled layout the tensor cores read; unused slots
+//           are zero-filled.  The ring is panel-major, so consecutive stages
+//           of a window form one contiguous operand;
+//   GEMM 1  S[64 heads, kKeys] = Q . K^T      tcgen05, M = 64, N = kKeys, K = 576
+//           (Q: nine TMA-loaded panels, resident for the whole block).  The
+//           tensor pipe is fed from shared memory, so its rate follows the
+//           operand bytes per MMA; the ring keeps several stages in flight;
+//   softmax one thread per head reads its S row from tensor memory: masked,
+//           scaled (log2 e folded in), exponentiated against a per-head
+//           reference max, row-summed, and written as bf16 P^T rows;
+//   GEMM 2  O^T[512 dims, 64 heads] += V^T . P^T  tcgen05, M = 128 (4 chunks of
+//           128 dims), N = 64, K = kKeys; V^T is read from the gathered
+//           panels 0..7 as an MN-major operand (no transpose pass).
+// The reference max only moves when a head's tile max exceeds it by more than
+// 2^8 (log2 units); then the block rescales that head's O^T column and its
+// running sum.  Anything in between stays within fp32 range, and the final
+// O / l is the same for every choice of reference.
+//
+// Warp roles (kThreads threads, one block per SM; more than 8 warps puts three
+// on some scheduler, which caps a thread at 168 registers):
+//   producers  rows w, w + kProducerWarps, ... of each stage; warp 0 also
+//              loads the query panels by TMA;
+//   next warp  tensor-memory allocation and MMA issue (one thread);
+//   last 4     softmax, O^T rescale, epilogue; warp w owns TMEM lanes
+//              32*(w%4)..+31: heads 16*(w%4)..+15 of S (an M = 64 result
+//              sits in lanes 0-15 of each 32-lane quarter) and dims
+//              128c + 32*(w%4)..+31 of O^T chunk c.
+// Tensor memory: O^T in columns 0-255 (chunk c at 64c), S in two buffers of
+// kKeys columns from 256.
+// The epilogue stages the block's result in the (then idle) gather buffers
+// and writes it with coalesced 16-byte stores: bf16 and normalised with one
+// split, else the unnormalised fp32 partial plus (reference max, sum) per
+// head for the combine kernel.
+#pragma once
+
+#include "common.cuh"
+#include "sparse_mla.cuh"
+
+namespace dsa {
+namespace mla {
+
+using attn::kMaxLayers;
+using attn::Params;
+
+constexpr int kH = 64;
+constexpr int kDv = 512;
+constexpr int kKeys = 64;                            // keys per window (GEMM 1 N, GEMM 2 K)
+constexpr int kStageRows = 32;                       // rows per gather stage
+constexpr int kStages = 4;                           // gather stages in the ring
+constexpr int kWinStages = kKeys / kStageRows;       // gather stages per window
+constexpr int kWindows = kStages / kWinStages;       // windows in the ring
+constexpr int kHalves = kKeys / 32;                  // 32-column TMEM loads per S row
+constexpr int kRingRows = kStages * kStageRows;      // 128
+constexpr int kPanels = 9;                           // 576 dims / 64
+constexpr int kPanelBytes = kRingRows * 128;         // one 64-dim panel of the ring: 16 KB
+constexpr int kRingBytes = kPanels * kPanelBytes;    // 147456
+constexpr int kQBytes = kPanels * kH * 128;          // 73728
+constexpr int kPBytes = kH * 128;                    // 64 heads x 64 keys bf16
+constexpr int kProducerWarps = 4;
+constexpr int kMmaWarp = kProducerWarps;
+constexpr int kSoftmaxWarp0 = kProducerWarps + 1;
+constexpr int kThreads = 32 * (kProducerWarps + 1 + 4);
+constexpr int kTmemCols = 512;
+constexpr int kOCol = 0;
+constexpr int kSCol = 256;
+constexpr int kSmallBytes = 1024;
+constexpr int kSmemBytes = 1024 + kQBytes + kRingBytes + kPBytes + kSmallBytes;
+static_assert(kSmemBytes <= 232448, "shared memory per block");
+static_assert(kRingBytes >= kH * kDv * 4, "the epilogue stages an fp32 partial in the gather ring");
+static_assert(kKeys % kStageRows == 0 && kStages % kWinStages == 0 && kKeys % 32 == 0, "windows tile the ring");
+constexpr float kRescaleLog2 = 8.0f;                 // rescale when the max grows by > 2^8
+
+struct Maps {
+  CUtensorMap q[kMaxLayers];   // [rows*64, 576] bf16, box 64 x 64, 128-byte swizzle
+};
+
+// Instruction descriptor, kind::f16, fp32 accumulate, bf16 operands.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major ? (1u << 15) : 0u) | (b_mn_major ? (1u << 16) : 0u) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Shared-memory descriptor of a 128-byte-swizzled operand.  K-major: rows of
+// 128 B (64 K-elements), 8-row groups `sbo` bytes apart.  MN-major: 64
+// MN-elements per 128-byte row, the next 64 MN-elements `lbo` bytes on, K rows
+// 128 B apart in 8-row groups `sbo` bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The mbarrier receives one arrival (no pending-count increment) once every
+// cp.async this thread issued before has landed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 8 columns, load (waited) and store.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the verdict goes to every lane.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Raw content of index slot `slot` of a row (-1 past k).  The load is only
+// issued here; nothing reads the value until checked_pos, tiles later.
+__device__ __forceinline__ int slot_raw(const int32_t *irow, int slot, int K) {
+  return slot < K ? __ldg(irow + slot) : -1;
+}
+// The position a raw slot names, or -1 when unused or out of range (an
+// out-of-range index is reported when `report`).
+__device__ __forceinline__ int checked_pos(int raw, int T, bool report) {
+  if (raw < -1 || raw >= T) {
+    if (report) raise_error(kErrDeviceCheck);
+    return -1;
+  }
+  return raw;
+}
+
+struct Small {
+  alignas(16) float xa[2][kH];    // per-head rescale factors (1/l for the epilogue)
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t s_full[2];
+  uint64_t s_empty[2];
+  uint64_t p_full;
+  uint64_t p_free;
+  uint64_t q_full;
+  uint64_t mma_done;
+  uint32_t tmem_slot;
+  int abort;
+  int status[2][4];               // per softmax warp, per iteration parity: 1 = ok
+  int need[2][4];                 // per softmax warp: a head of it moves its reference max
+};
+static_assert(sizeof(Small) <= kSmallBytes, "small shared region");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sQ = base;                                  // [9 panels][64 heads][128 B]
+  uint8_t *sK = sQ + kQBytes;                          // [9 panels][128 ring rows][128 B]
+  uint8_t *sP = sK + kRingBytes;                       // [64 heads][128 B]: P^T, K-major
+  Small *sm = reinterpret_cast<Small *>(sP + kPBytes);
+  volatile int *abort_flag = &sm->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int nl = p.n_layers;
+  const int layer = blockIdx.x % nl;
+  const int rest = blockIdx.x / nl;
+  const int split = rest % p.nsplit;
+  const int row = rest / p.nsplit;
+  const int b = row / p.Q;
+  const int slot0 = split * p.blocks_per_split * kKeys;
+  int nblk = p.blocks_per_split;
+  {
+    const int remaining = (p.K - slot0 + kKeys - 1) / kKeys;
+    nblk = remaining < nblk ? remaining : nblk;
+    if (nblk < 0) nblk = 0;
+  }
+  const int32_t *irow = p.idx + (size_t)row * p.K;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sm->full[i], 32 * kProducerWarps);
+      mbar_init(&sm->empty[i], 1);
+    }
+    // (a window j uses stages 2*(j%2) and 2*(j%2)+1)
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm->s_full[i], 1);
+      mbar_init(&sm->s_empty[i], 4);
+    }
+    mbar_init(&sm->p_full, 4);
+    mbar_init(&sm->p_free, 1);
+    mbar_init(&sm->q_full, 1);
+    mbar_init(&sm->mma_done, 1);
+    sm->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) prefetch_tensormap(&maps.q[layer]);
+  if (warp == kMmaWarp) tmem_alloc(&sm->tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sm->tmem_slot;
+
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------------------ producers
+    bool q_issued = false;
+    if (warp == 0 && nblk > 0) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&sm->q_full, kQBytes);
+        for (int pp = 0; pp < kPanels; ++pp)
+          tma_load_2d(sQ + pp * kH * 128, &maps.q[layer], pp * 64, row * kH, &sm->q_full);
+      }
+      q_issued = true;
+    }
+    const uint8_t *kvb = reinterpret_cast<const uint8_t *>(p.kv[layer]) + (size_t)b * p.T * (kDv + 64) * 2;
+    // gather stage g (g = 0, 1, ...) holds index slots 32g..32g+31 of this block
+    // in ring stage g % 4; lane l holds slot l of stage g, loaded three stages ahead
+    const int nstage = nblk * kWinStages;
+    auto load_slot = [&](int g) -> int { return g < nstage ? slot_raw(irow, slot0 + g * kStageRows + lane, p.K) : -1; };
+    int n1 = load_slot(0), n2 = load_slot(1), n3 = load_slot(2);
+    for (int g = 0; g < nstage; ++g) {
+      const int cur = checked_pos(n1, p.T, warp == 0);
+      n1 = n2;
+      n2 = n3;
+      n3 = load_slot(g + 3);
+      const int s = g % kStages;
+      const uint32_t ph = static_cast<uint32_t>(g / kStages) & 1u;
+      if (!warp_wait(&sm->empty[s], ph ^ 1u, abort_flag)) break;
+      const uint32_t sbase = smem_u32(sK) + s * kStageRows * 128;
+      for (int r = warp; r < kStageRows; r += kProducerWarps) {
+        const int pos = __shfl_sync(0xffffffffu, cur, r);
+        const uint8_t *src = kvb + (size_t)(pos < 0 ? 0 : pos) * ((kDv + 64) * 2);
+        const uint32_t nbytes = pos < 0 ? 0u : 16u;  // unused slot: zero-filled row
+        const uint32_t rbase = sbase + r * 128;       // ring row s*32 + r; (s*32 + r) % 8 == r % 8
+#pragma unroll
+        for (int cc = 0; cc < 3; ++cc) {
+          const int c = lane + 32 * cc;  // 16-byte chunk of the 1152-byte row
+          if (c < 72) cp_async_16(rbase + (c >> 3) * kPanelBytes + (((c & 7) ^ (r & 7)) << 4), src + c * 16, nbytes);
+        }
+      }
+      cp_async_mbar_arrive(&sm->full[s]);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (q_issued && lane == 0) mbar_wait_drain(&sm->q_full, 0, kWaitLimitNs);
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nblk > 0) {
+      constexpr uint32_t id1 = idesc(64, kKeys, false, false);
+      constexpr uint32_t id2 = idesc(128, 64, true, false);
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), p0 = smem_u32(sP);
+      bool ok = mbar_wait_bounded(&sm->q_full, 0, abort_flag);
+      // Issue whichever is ready: GEMM 2 of window g2 once its P is written
+      // (first: it unblocks the softmax), else GEMM 1 of window g1 once its
+      // rows have landed and its S buffer is free.  A fixed order would let a
+      // window still being gathered hold up the softmax of the previous one.
+      int g1 = 0, g2 = 0;
+      unsigned long long t_idle = 0;
+      while (ok && g2 < nblk) {
+        bool progressed = false;
+        if (g2 < g1 && mbar_try_wait(&sm->p_full, static_cast<uint32_t>(g2) & 1u)) {
+          tc_fence_after();
+          const int w = g2 % kWindows;
+          const uint32_t ks = k0 + w * kKeys * 128;
+#pragma unroll
+          for (int c = 0; c < kDv / 128; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < kKeys / 16; ++kk) {
+              const uint64_t ad = desc_sw128(ks + 2 * c * kPanelBytes + kk * 16 * 128, kPanelBytes, 1024);
+              const uint64_t bd = desc_sw128(p0 + kk * 32, 16, 1024);
+              tc_mma_bf16(tmem_base + kOCol + c * 64, ad, bd, id2, (g2 > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          for (int h = 0; h < kWinStages; ++h) tc_commit(&sm->empty[w * kWinStages + h]);
+          tc_commit(&sm->p_free);
+          ++g2;
+          progressed = true;
+        } else if (g1 < nblk) {
+          const int w = g1 % kWindows;  // window slot in the ring
+          const int sb = g1 & 1;        // S buffer
+          const uint32_t ph = static_cast<uint32_t>(g1 / kWindows) & 1u;
+          bool ready = mbar_try_wait(&sm->s_empty[sb], (static_cast<uint32_t>(g1 >> 1) & 1u) ^ 1u);
+          for (int h = 0; h < kWinStages && ready; ++h) ready = mbar_try_wait(&sm->full[w * kWinStages + h], ph);
+          if (ready) {
+            fence_proxy_async_smem();  // the gathered rows were written by cp.async (generic proxy)
+            tc_fence_after();
+            const uint32_t d = tmem_base + kSCol + sb * kKeys;
+            const uint32_t ks = k0 + w * kKeys * 128;  // the window's rows in every panel
+#pragma unroll
+            for (int kk = 0; kk < kPanels * 4; ++kk) {
+              const uint32_t qoff = (kk >> 2) * (kH * 128) + (kk & 3) * 32;
+              const uint32_t koff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+              tc_mma_bf16(d, desc_sw128(q0 + qoff, 16, 1024), desc_sw128(ks + koff, 16, 1024), id1, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(&sm->s_full[sb]);
+            ++g1;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_idle = 0;
+        } else {
+          const unsigned long long now = global_timer_ns();
+          if (t_idle == 0) {
+            t_idle = now;
+          } else if (*abort_flag) {
+            ok = false;
+          } else if (now - t_idle > kWaitLimitNs) {
+            raise_error(kErrTimeout);
+            *abort_flag = 1;
+            ok = false;
+          }
+        }
+      }
+      tc_commit(&sm->mma_done);
+      mbar_wait_drain(&sm->mma_done, 0, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int q4 = warp & 3;                         // TMEM lane quarter of this warp
+    const int w4 = warp - kSoftmaxWarp0;             // index among the softmax warps
+    const int head = q4 * 16 + lane;                 // meaningful for lane < 16
+    const bool owner = lane < 16;
+    const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
+    float m_ref = -INFINITY, l = 0.0f;
+    bool all_ok = true;
+    // validity of window j's keys (bit k of word h = key 32h + k), from the
+    // index set itself; slots are loaded two windows ahead, checked when used
+    auto load_slot = [&](int j, int h) -> int {
+      return j < nblk ? slot_raw(irow, slot0 + j * kKeys + h * 32 + lane, p.K) : -1;
+    };
+    int n1[kHalves], n2[kHalves];
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h) {
+      n1[h] = load_slot(0, h);
+      n2[h] = load_slot(1, h);
+    }
+    for (int j = 0; j < nblk; ++j) {
+      const int sb = j & 1;
+      uint32_t mask[kHalves];
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h) {
+        mask[h] = __ballot_sync(0xffffffffu, checked_pos(n1[h], p.T, false) >= 0);
+        n1[h] = n2[h];
+        n2[h] = load_slot(j + 2, h);
+      }
+      bool ok = warp_wait(&sm->s_full[sb], static_cast<uint32_t>(j >> 1) & 1u, abort_flag);
+      uint32_t sv[kKeys];  // raw scores, then (in place) scaled and masked logits
+      float mt = -INFINITY;
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < kHalves; ++h)
+          tmem_ld_32x32b_x32_nowait(tmem_base + lane_addr + kSCol + sb * kKeys + 32 * h,
+                                    *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * h));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->s_empty[sb]);
+#pragma unroll
+        for (int k = 0; k < kKeys; ++k) {
+          const float v = ((mask[k >> 5] >> (k & 31)) & 1u) ? __uint_as_float(sv[k]) * p.scale_log2 : -INFINITY;
+          sv[k] = __float_as_uint(v);
+          mt = fmaxf(mt, v);
+        }
+      }
+      const bool need = ok && owner && mt > m_ref + kRescaleLog2;
+      const float m_new = need ? mt : m_ref;
+      const float alpha = need ? exp2f(m_ref - m_new) : 1.0f;
+      // this window's probabilities against the (possibly moved) reference,
+      // packed to bf16 now so the logits are dead before any O^T rescale
+      uint32_t pk[kKeys / 2];
+      float rs = 0.0f;
+      if (ok && owner) {
+        const float ref = m_new == -INFINITY ? 0.0f : m_new;
+#pragma unroll
+        for (int e = 0; e < kKeys / 2; ++e) {
+          const float a = exp2f(__uint_as_float(sv[2 * e]) - ref);
+          const float bq = exp2f(__uint_as_float(sv[2 * e + 1]) - ref);
+          rs += a + bq;
+          pk[e] = pack_bf16x2(a, bq);
+        }
+      }
+      if (ok && j > 0) ok = warp_wait(&sm->p_free, static_cast<uint32_t>(j - 1) & 1u, abort_flag);
+      const unsigned any_need = __ballot_sync(0xffffffffu, need);
+      if (owner) sm->xa[j & 1][head] = alpha;
+      if (lane == 0) {
+        sm->status[j & 1][w4] = ok ? 1 : 0;
+        sm->need[j & 1][w4] = any_need ? 1 : 0;
+      }
+      named_bar_sync(1, 128);
+      all_ok = sm->status[j & 1][0] && sm->status[j & 1][1] && sm->status[j & 1][2] && sm->status[j & 1][3];
+      if (!all_ok) break;
+      const bool rescale = sm->need[j & 1][0] || sm->need[j & 1][1] || sm->need[j & 1][2] || sm->need[j & 1][3];
+      if (rescale && j > 0) {
+        // O^T column h *= alpha[h] on this warp's 32 lanes of every chunk
+        // (rare: 8 columns at a time keeps the registers of the hot path free)
+        tc_fence_after();
+#pragma unroll 1
+        for (int g = 0; g < (kDv / 128) * (kH / 8); ++g) {
+          const int c = g / (kH / 8), h0 = (g % (kH / 8)) * 8;
+          const uint32_t taddr = tmem_base + lane_addr + kOCol + c * 64 + h0;
+          uint32_t r[8];
+          tmem_ld8(taddr, r);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * sm->xa[j & 1][h0 + i]);
+          tmem_st8(taddr, r);
+        }
+        tmem_wait_st();
+      }
+      if (need) {
+        m_ref = m_new;
+        l *= alpha;
+      }
+      if (owner) {
+        uint8_t *prow = sP + head * 128;
+#pragma unroll
+        for (int c = 0; c < kKeys / 8; ++c)
+          *reinterpret_cast<uint4 *>(prow + ((c ^ (head & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        l += rs;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->p_full);
+    }
+
+    // ---- epilogue: O^T / l per head, staged in the idle gather buffers
+    bool ok = all_ok;
+    if (nblk > 0 && ok) ok = warp_wait(&sm->p_free, static_cast<uint32_t>(nblk - 1) & 1u, abort_flag);
+    float *inv_l = sm->xa[0];
+    named_bar_sync(1, 128);  // every warp is past its last read of xa
+    if (owner) inv_l[head] = l > 0.0f ? 1.0f / l : 0.0f;
+    if (lane == 0) sm->status[0][w4] = ok ? 1 : 0;
+    named_bar_sync(1, 128);
+    ok = sm->status[0][0] && sm->status[0][1] && sm->status[0][2] && sm->status[0][3];
+    // After the last GEMM 2 every gather and MMA of this block is complete, so
+    // the stage buffers are free; on an abort they may not be, so stay out.
+    const size_t rowL = (size_t)layer * p.rows + row;
+    const bool one = p.nsplit == 1;
+    if (owner) {
+      if (one) {
+        if (p.lse[layer] != nullptr) {
+          const float ln2 = 0.69314718055994531f;
+          p.lse[layer][(size_t)row * kH + head] = (ok && l > 0.0f) ? (m_ref + log2f(l)) * ln2 : -INFINITY;
+        }
+      } else {
+        float *pm = p.part_ml + ((rowL * p.nsplit + split) * kH) * 2;
+        pm[head * 2 + 0] = ok ? m_ref : -INFINITY;
+        pm[head * 2 + 1] = ok ? l : 0.0f;
+      }
+    }
+    const int tid = threadIdx.x - 32 * kSoftmaxWarp0;  // 0..127
+    if (ok && nblk > 0) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < kDv / 128; ++c) {
+        const int d = c * 128 + q4 * 32 + lane;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32_nowait(tmem_base + lane_addr + kOCol + c * 64 + hh * 32, r);
+          tmem_wait_ld();
+          if (one) {
+            __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sK);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              stg[(hh * 32 + i) * kDv + d] = __float2bfloat16_rn(__uint_as_float(r[i]) * inv_l[hh * 32 + i]);
+          } else {
+            float *stg = reinterpret_cast<float *>(sK);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) stg[(hh * 32 + i) * kDv + d] = __uint_as_float(r[i]);
+          }
+        }
+      }
+      named_bar_sync(1, 128);
+      const uint4 *src = reinterpret_cast<const uint4 *>(sK);
+      uint4 *dst = one ? reinterpret_cast<uint4 *>(p.out[layer] + (size_t)row * kH * kDv)
+                       : reinterpret_cast<uint4 *>(p.part_o + ((rowL * p.nsplit + split) * kH) * kDv);
+      const int n16 = one ? kH * kDv * 2 / 16 : kH * kDv * 4 / 16;
+      for (int i = tid; i < n16; i += 128) dst[i] = src[i];
+    } else {
+      // no index in this slice, or the block gave up: zeros
+      uint4 *dst = one ? reinterpret_cast<uint4 *>(p.out[layer] + (size_t)row * kH * kDv)
+                       : reinterpret_cast<uint4 *>(p.part_o + ((rowL * p.nsplit + split) * kH) * kDv);
+      const int n16 = one ? kH * kDv * 2 / 16 : kH * kDv * 4 / 16;
+      for (int i = tid; i < n16; i += 128) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace mla
+}  // namespace dsa
