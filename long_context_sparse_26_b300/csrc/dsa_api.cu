@@ -19,6 +19,11 @@ namespace {
 
 using dsa::attn::kMaxLayers;
 
+// The indexer counts the top-k's first digit: both sides must agree on it.
+static_assert(dsa::indexer::kHistBins == dsa::topk::kBins0 && dsa::indexer::kHistShift == dsa::topk::kShift0 &&
+                  dsa::indexer::kHistRowStride == dsa::topk::kGhistStride,
+              "indexer histogram and top-k digit 0 disagree");
+
 constexpr int kIdxHeads = 64, kIdxDim = 128, kHeads = 64, kLora = 512, kRope = 64, kMaxTopk = 2048;
 constexpr int kMaxDevices = 64;
 constexpr long long kMaxRowsY = 65535;  // grid.y limit for (chunk, row) launches
@@ -134,6 +139,7 @@ TopkShape topk_shape(int rows, int T, int sms) {
   int n = (target + rows - 1) / rows;
   const int max_chunks = (T + 4095) / 4096;  // chunks of at least 4096 scores
   n = n < max_chunks ? n : max_chunks;
+  n = n < dsa::topk::kThreads ? n : dsa::topk::kThreads;  // the select block prefix-sums one count per thread
   n = n < 1 ? 1 : n;
   s.chunk = static_cast<int>(align_up((T + n - 1) / n, 1024));
   s.nchunk = (T + s.chunk - 1) / s.chunk;
@@ -166,7 +172,7 @@ AttnShape attn_shape(long long rowsL, int K, int sms) {
 }
 
 struct Layout {
-  size_t scores = 0, ghist = 0, gcount = 0, cand = 0, idx = 0, part_o = 0, part_ml = 0, total = 0;
+  size_t scores = 0, ghist = 0, plan = 0, counts = 0, cand = 0, idx = 0, part_o = 0, part_ml = 0, total = 0;
   TopkShape ts;
 };
 
@@ -187,12 +193,15 @@ Layout layout(int B, int Q, int T, int n_layers, int K, int sms) {
   size_t off = 0;
   L.scores = off;
   off = align_up(off + static_cast<size_t>(rows) * T * sizeof(float), 256);
-  // chunked top-k: digit histograms and candidate counters (zeroed by one
-  // memset, so they are adjacent), then room for T candidates per row
+  // chunked top-k: digit histograms, row plans and per-chunk candidate
+  // counts (zeroed by one memset, so they are adjacent), then room for T
+  // candidates per row
   L.ghist = off;
-  if (L.ts.nchunk > 1) off += static_cast<size_t>(rows) * 2 * dsa::topk::kBins * 4;
-  L.gcount = off;
-  if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(rows) * 4, 256);
+  if (L.ts.nchunk > 1) off += static_cast<size_t>(rows) * dsa::topk::kGhistStride * 4;
+  L.plan = off;
+  if (L.ts.nchunk > 1) off += static_cast<size_t>(rows) * 4 * 4;
+  L.counts = off;
+  if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(rows) * L.ts.nchunk * 2 * 4, 256);
   L.cand = off;
   if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(rows) * T * 8, 256);
   L.idx = off;
@@ -271,7 +280,8 @@ dsa_status_t launch_topk(const Layout &L, uint8_t *ws, const float *scores, cons
   p.chunk = L.ts.chunk;
   p.nchunk = L.ts.nchunk;
   p.ghist = reinterpret_cast<uint32_t *>(ws + L.ghist);
-  p.gcount = reinterpret_cast<uint32_t *>(ws + L.gcount);
+  p.plan = reinterpret_cast<uint32_t *>(ws + L.plan);
+  p.counts = reinterpret_cast<uint32_t *>(ws + L.counts);
   p.cand = reinterpret_cast<uint64_t *>(ws + L.cand);
   p.idx = idx;
   const dim3 grid(p.nchunk, rows);
@@ -279,6 +289,7 @@ dsa_status_t launch_topk(const Layout &L, uint8_t *ws, const float *scores, cons
     if (clear_topk_state(L, ws, stream) != DSA_OK) return DSA_ERR_CUDA;
     topk_chunk_hist_kernel<<<grid, kThreads, 0, stream>>>(p);
   }
+  topk_plan_kernel<<<rows, kThreads, 0, stream>>>(p);
   topk_chunk_scan_kernel<1><<<grid, kThreads, 0, stream>>>(p);
   topk_chunk_scan_kernel<2><<<grid, kThreads, 0, stream>>>(p);
   topk_chunk_select_kernel<<<rows, kThreads, kSelectSmem, stream>>>(p);

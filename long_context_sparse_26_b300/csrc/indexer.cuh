@@ -23,10 +23,12 @@
 // loaded; the epilogue writes -inf there.
 //
 // With one query per sequence (decode), the epilogue can also count each
-// visible score's top 11 key bits into a per-row histogram (the first step of
-// the top-k selection): each epilogue warp keeps its own shared-memory
-// histogram and adds it to the global one when its sequence changes, so the
-// count costs no extra pass over the scores and no cross-warp wait.
+// visible score's top 13 key bits into a per-row histogram (the first step of
+// the top-k selection), so the count costs no extra pass over the scores:
+// the four epilogue warps share one 8192-bin shared-memory histogram and add
+// it to the global one when the block's sequence changes.  The flush is
+// fenced on both sides by an mbarrier the four warps arrive on (a bounded
+// wait, so a block that gives up never strands a warp).
 #pragma once
 
 #include "common.cuh"
@@ -49,7 +51,7 @@ struct Cfg {
   static constexpr int kEpiWarps = QG == 4 ? 8 : 4;
   static constexpr int kQPW = QG * 4 / kEpiWarps;       // queries per epilogue warp
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr int kHistBytes = QG == 1 ? 4 * 2048 * 4 : 0;  // per-epilogue-warp digit-0 histograms
+  static constexpr int kHistBytes = QG == 1 ? 8192 * 4 : 0;   // the block's digit-0 histogram
   static constexpr int kAcc = QG == 4 ? 2 : 4;          // accumulator buffers in TMEM
   static constexpr int kTmemCols = (kAcc * N <= 256) ? 256 : 512;
   static constexpr int kSmall = 1024 + 4 * QG * kHeads * 4;  // barriers + flags, then per-warp weights
@@ -67,23 +69,41 @@ struct Params {
   int ntiles;            // ceil(T / 128)
   long long units;       // B * ngroups * ntiles
   int stream_keys;       // 1: every key tile is read once (evict-first in L2)
-  uint32_t *ghist;       // QG == 1 only, may be null: [B][2][2048] digit-0 histograms (first half of each row)
+  uint32_t *ghist;       // QG == 1 only, may be null: [B][8192 + 2048], digit-0 histogram in the first 8192
 };
 
-constexpr int kHistBins = 2048;
-constexpr int kHistShift = 21;
+constexpr int kHistBins = 8192;          // digit 0 of the top-k: key bits 31..19
+constexpr int kHistShift = 19;
+constexpr int kHistRowStride = 8192 + 2048;  // per-row words of the global histograms
 
-// Adds a warp's shared histogram to row `row` of the global one and clears it.
-__device__ __forceinline__ void flush_hist(uint32_t *whist, uint32_t *ghist, int row, int lane) {
-  uint32_t *g = ghist + (size_t)row * 2 * kHistBins;
-  for (int i = lane; i < kHistBins; i += 32) {
-    const uint32_t c = whist[i];
+// Epilogue warp e's quarter of the block histogram is added to row `row` of
+// the global one and cleared, between two rounds on `bar` (four arrivals a
+// round: every warp is done counting before anyone flushes, and done
+// flushing before anyone counts again).  False if the block gave up.
+__device__ __forceinline__ bool flush_hist(uint32_t *hist, uint32_t *ghist, int row, int e, int lane, uint64_t *bar,
+                                           uint32_t &bar_phase, volatile int *abort) {
+  int ok = 1;
+  if (lane == 0) {
+    mbar_arrive(bar);
+    ok = mbar_wait_bounded(bar, bar_phase, abort) ? 1 : 0;
+  }
+  bar_phase ^= 1u;
+  if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+  uint32_t *g = ghist + (size_t)row * kHistRowStride;
+  for (int i = e * (kHistBins / 4) + lane; i < (e + 1) * (kHistBins / 4); i += 32) {
+    const uint32_t c = hist[i];
     if (c) {
       atomicAdd(g + i, c);
-      whist[i] = 0;
+      hist[i] = 0;
     }
   }
   __syncwarp();
+  if (lane == 0) {
+    mbar_arrive(bar);
+    ok = mbar_wait_bounded(bar, bar_phase, abort) ? 1 : 0;
+  }
+  bar_phase ^= 1u;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // Largest visible position of a query group (-1 if none), clamped to [-1, T-1].
@@ -118,12 +138,13 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
   uint64_t *bfull = tempty + C::kAcc;
   uint64_t *bfree = bfull + 1;
   uint64_t *mma_done = bfree + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+  uint64_t *hist_bar = mma_done + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(hist_bar + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   // [epilogue warps][queries per warp][64]: each epilogue warp keeps its own
   // copy of its queries' head weights, so the warps never wait on one another.
   float *sw_all = reinterpret_cast<float *>(small + 1024);
-  uint32_t *hist_all = reinterpret_cast<uint32_t *>(small + C::kSmall);  // QG == 1: [4 warps][2048]
+  uint32_t *hist = reinterpret_cast<uint32_t *>(small + C::kSmall);  // QG == 1: [8192]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -143,6 +164,7 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
     mbar_init(bfull, 1);
     mbar_init(bfree, 1);
     mbar_init(mma_done, 1);
+    mbar_init(hist_bar, 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -151,6 +173,8 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
     prefetch_tensormap(&tmap_q);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  if (QG == 1 && p.ghist != nullptr)
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -262,12 +286,8 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
     const int quarter = warp & 3;                  // TMEM lanes this warp may read
     const int qb = (e >> 2) * QPW;                 // first query (within the group) of this warp
     float *sw = sw_all + e * QPW * kHeads;
-    uint32_t *whist = hist_all + (e & 3) * kHistBins;
     const bool do_hist = QG == 1 && p.ghist != nullptr;
-    if (do_hist) {
-      for (int i = lane; i < kHistBins; i += 32) whist[i] = 0;
-      __syncwarp();
-    }
+    uint32_t hist_phase = 0;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -280,7 +300,8 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
       const long long seg = u / p.ntiles;
       const int tile = static_cast<int>(u - seg * p.ntiles);
       if (seg != cur_seg) {
-        if (do_hist && cur_seg >= 0) flush_hist(whist, p.ghist, b, lane);
+        if (do_hist && cur_seg >= 0 && !flush_hist(hist, p.ghist, b, e, lane, hist_bar, hist_phase, abort_flag))
+          break;
         b = static_cast<int>(seg / p.ngroups);
         q0 = static_cast<int>(seg - (long long)b * p.ngroups) * QG;
         seg_max = group_max_pos<QG>(p, b, q0);
@@ -318,28 +339,48 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
           // both 32-column halves of the query's 64 heads, one wait
           const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * C::N + (qb + i) * kHeads);
           const float4 *w4 = reinterpret_cast<const float4 *>(sw + i * kHeads);
-          uint32_t v0[32], v1[32];
-          tmem_ld_32x32b_x32_nowait(taddr, v0);
-          tmem_ld_32x32b_x32_nowait(taddr + 32, v1);
-          tmem_wait_ld();
-          float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent chains
+          if constexpr (QG == 1) {
+            // decode: each 32-column half is loaded and reduced in turn (the
+            // key stream, not this epilogue, sets the pace here)
+            float v[32];
+            float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-          for (int j = 0; j < 64; j += 4) {
-            const float4 wv = w4[j >> 2];
-            const uint32_t *v = j < 32 ? v0 + j : v1 + (j - 32);
-            const int c = (j >> 2) & 1;
-            a[4 * c + 0] = fmaf(wv.x, fmaxf(__uint_as_float(v[0]), 0.0f), a[4 * c + 0]);
-            a[4 * c + 1] = fmaf(wv.y, fmaxf(__uint_as_float(v[1]), 0.0f), a[4 * c + 1]);
-            a[4 * c + 2] = fmaf(wv.z, fmaxf(__uint_as_float(v[2]), 0.0f), a[4 * c + 2]);
-            a[4 * c + 3] = fmaf(wv.w, fmaxf(__uint_as_float(v[3]), 0.0f), a[4 * c + 3]);
+            for (int h = 0; h < 2; ++h) {
+              tmem_ld_32x32b_x32(taddr + h * 32, v);
+#pragma unroll
+              for (int j = 0; j < 32; j += 4) {
+                const float4 wv = w4[(h * 32 + j) >> 2];
+                s0 = fmaf(wv.x, fmaxf(v[j + 0], 0.0f), s0);
+                s1 = fmaf(wv.y, fmaxf(v[j + 1], 0.0f), s1);
+                s0 = fmaf(wv.z, fmaxf(v[j + 2], 0.0f), s0);
+                s1 = fmaf(wv.w, fmaxf(v[j + 3], 0.0f), s1);
+              }
+            }
+            s = s0 + s1;
+          } else {
+            uint32_t v0[32], v1[32];
+            tmem_ld_32x32b_x32_nowait(taddr, v0);
+            tmem_ld_32x32b_x32_nowait(taddr + 32, v1);
+            tmem_wait_ld();
+            float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent chains
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+              const float4 wv = w4[j >> 2];
+              const uint32_t *v = j < 32 ? v0 + j : v1 + (j - 32);
+              const int c = (j >> 2) & 1;
+              a[4 * c + 0] = fmaf(wv.x, fmaxf(__uint_as_float(v[0]), 0.0f), a[4 * c + 0]);
+              a[4 * c + 1] = fmaf(wv.y, fmaxf(__uint_as_float(v[1]), 0.0f), a[4 * c + 1]);
+              a[4 * c + 2] = fmaf(wv.z, fmaxf(__uint_as_float(v[2]), 0.0f), a[4 * c + 2]);
+              a[4 * c + 3] = fmaf(wv.w, fmaxf(__uint_as_float(v[3]), 0.0f), a[4 * c + 3]);
+            }
+            s = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
           }
-          s = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
         }
         if (key < p.T) {
           float *row = p.scores + ((size_t)b * p.Q + q0 + qb + i) * (size_t)p.T;
           const bool vis = real && key <= posv[i];
           row[key] = vis ? s : -INFINITY;
-          if (do_hist && vis) atomicAdd(&whist[score_key(s) >> kHistShift], 1u);
+          if (do_hist && vis) atomicAdd(&hist[score_key(s) >> kHistShift], 1u);
         }
       }
       if (real) {
@@ -352,7 +393,7 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
         }
       }
     }
-    if (do_hist && cur_seg >= 0) flush_hist(whist, p.ghist, b, lane);
+    if (do_hist && cur_seg >= 0 && !*abort_flag) flush_hist(hist, p.ghist, b, e, lane, hist_bar, hist_phase, abort_flag);
   }
 
   tc_fence_before();

@@ -73,7 +73,7 @@ constexpr int kPanelBytes = kRingRows * 128;         // one 64-dim panel of the 
 constexpr int kRingBytes = kPanels * kPanelBytes;    // 147456
 constexpr int kQBytes = kPanels * kH * 128;          // 73728
 constexpr int kPBytes = kH * 128;                    // 64 heads x 64 keys bf16
-constexpr int kProducerWarps = 4;
+constexpr int kProducerWarps = 7;
 constexpr int kMmaWarp = kProducerWarps;
 constexpr int kSoftmaxWarp0 = kProducerWarps + 1;
 constexpr int kThreads = 32 * (kProducerWarps + 1 + 4);

@@ -9,27 +9,36 @@
 // composite (key << 32 | ~position), whose descending order is exactly
 // "score desc, position asc".  The k largest composites are the selection.
 //
-//   1. histogram of the top 11 key bits (digit 0) over the row -> the bin b0
-//      holding the k-th largest key;
-//   2. pass 1 over the row: every position with digit 0 > b0 is a candidate;
-//      positions in bin b0 feed a histogram of the next 11 bits (digit 1);
-//   3. pass 2 over the row: positions in bin b0 whose digit 1 is >= b1 (the
-//      sub-bin holding the k-th key) are candidates too;
-//   4. radix select over the ~k candidates' composites gives the exact k-th
-//      composite tau; the k positions with composite >= tau are sorted
-//      ascending (bitonic, in shared memory) and written.
-// Every count is an integer and the final order comes from a sort, so the
-// result does not depend on thread scheduling.
+//   1. histogram of the top 13 key bits (digit 0: sign, exponent and 4
+//      mantissa bits, i.e. bins 1/16 of an octave wide) over the row -> the
+//      bin b0 holding the k-th largest key, the count above it and its own;
+//   2. pass 1 over the row: every position with digit 0 > b0 is a candidate,
+//      and so is all of bin b0 when it fits beside them in the select
+//      buffer (the usual case: a row's threshold bin then holds a few
+//      thousand scores, 1M-score rows included); otherwise bin b0 feeds a
+//      histogram of the next 11 bits (digit 1) and
+//   3. pass 2 over the row takes the positions of bin b0 whose digit 1 is at
+//      or above the sub-bin b1 holding the k-th key;
+//   4. radix select over the candidates' composites gives the exact k-th
+//      composite tau; exactly k candidates have composite >= tau.
+// Candidates are kept in position order (block-wide prefix sums, no
+// atomics), so after a single-pass row the k winners come out ascending by an
+// ordered compaction; after two passes they are sorted (bitonic, in shared
+// memory).  Every count is an integer and every order comes from a prefix
+// or a sort, so the result does not depend on thread scheduling.
 //
 // Two launch shapes:
 //   * many rows (prefill): one block per row does every step in shared memory;
-//   * few long rows (decode): (chunk, row) blocks do steps 1-3 and append
-//     candidates to a global buffer (one atomic per block), then one block per
-//     row does step 4.  Step 1 may come fused from the indexer.  Passes are
+//   * few long rows (decode): (chunk, row) blocks count step 1 (or it comes
+//     fused from the indexer), one block per row reads the histogram once and
+//     writes the row's plan (b0, need, whether bin b0 is taken whole), then
+//     (chunk, row) blocks do steps 2-3, each writing its candidates in order
+//     into its own chunk's slice of a per-row buffer plus a count, and one
+//     block per row gathers the chunks in order and does step 4.  Passes are
 //     separate launches in stream order; no block waits on another.
-// If a row's candidates overflow the shared-memory buffer (e.g. thousands of
-// exactly equal scores), the one-block-per-row path falls back to three
-// exact radix passes over the row and an ordered write.
+// If a row still has more candidates than the select buffer holds (thousands
+// of exactly equal scores), three exact radix passes over the row and an
+// ordered write replace step 4.
 #pragma once
 
 #include "common.cuh"
@@ -38,16 +47,17 @@ namespace dsa {
 namespace topk {
 
 constexpr int kThreads = 512;
-constexpr int kBins = 2048;          // 11-bit digits
-constexpr int kShift0 = 21;          // digit 0: key bits 31..21
-constexpr int kShift1 = 10;          // digit 1: key bits 20..10
+constexpr int kBins0 = 8192;         // digit 0: key bits 31..19
+constexpr int kShift0 = 19;
+constexpr int kBins = 2048;          // digit 1 (key bits 18..8) and the radix passes of the select
+constexpr int kShift1 = 8;
 constexpr int kSortN = 2048;         // bitonic sort size (>= the largest k)
-constexpr int kSmemCand = 11776;     // composites held in shared memory (92 KB: two blocks per SM)
-constexpr int kBlockCand = 2048;     // candidates a chunk block stages before its one global append
+constexpr int kSmemCand = 8192;      // composites held in shared memory (64 KB: two blocks per SM)
 constexpr int kUnroll = 8;
 
-// dynamic shared memory of the select and row kernels
-constexpr int kSelectSmem = kSmemCand * 8 + kBins * 4 + kSortN * 4;
+// dynamic shared memory of the select and row kernels: candidates, a
+// histogram of up to kBins0 bins, the sort buffer
+constexpr int kSelectSmem = kSmemCand * 8 + kBins0 * 4 + kSortN * 4;
 
 __device__ __forceinline__ int visible_length(const int32_t *q_pos, int row, int T) {
   const int pos = __ldg(q_pos + row);
@@ -73,9 +83,10 @@ struct Scratch {
 // count, finds the bin b with count(bins > b) < need <= count(bins >= b).
 // Writes b to sc->result[0], need - count(bins > b) to result[1] and the bin's
 // own count to result[2].  Called by every thread; ends with the result visible.
+template <int NBINS = kBins>
 __device__ void find_threshold_bin(const uint32_t *hist, uint32_t need, Scratch *sc) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  constexpr int per = kBins / kThreads;  // 4 bins per thread
+  constexpr int per = NBINS / kThreads;  // bins per thread
   uint32_t h[per];
   uint32_t ts = 0;
 #pragma unroll
@@ -125,35 +136,28 @@ __device__ __forceinline__ uint32_t block_prefix(bool flag, uint32_t *total, Scr
   return before + in_warp;
 }
 
-// Where candidates go: a shared-memory list of `cap` entries whose counter is
-// sc->count; entries beyond it go straight to a global list (`gdst`, counter
-// `gcount`, capacity `gcap`) when one is given, else they are only counted.
-struct Sink {
-  uint64_t *list;
-  uint32_t cap;
-  uint64_t *gdst;
-  uint32_t *gcount;
-  uint32_t gcap;
-};
-
-// Warp-aggregated append of `v` for every lane with take == true.  Every lane
-// of the warp must call it.
-__device__ __forceinline__ void sink_append(const Sink &s, Scratch *sc, bool take, uint64_t v) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t bal = __ballot_sync(0xffffffffu, take);
-  if (bal == 0) return;
-  const int leader = __ffs(bal) - 1;
-  uint32_t base = 0;
-  if (lane == leader) base = atomicAdd(&sc->count, static_cast<uint32_t>(__popc(bal)));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  if (!take) return;
-  const uint32_t slot = base + __popc(bal & ((1u << lane) - 1u));
-  if (slot < s.cap) {
-    s.list[slot] = v;
-  } else if (s.gdst != nullptr) {
-    const uint32_t g = atomicAdd(s.gcount, 1u);
-    if (g < s.gcap) s.gdst[g] = v;
+// Block-wide exclusive prefix sum of small per-thread counts, in thread order,
+// plus the total.  Every thread calls it.
+__device__ __forceinline__ uint32_t block_exclusive_sum(uint32_t v, uint32_t *total, Scratch *sc) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
   }
+  if (lane == 31) sc->warp_b[warp] = x;
+  __syncthreads();
+  uint32_t before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const uint32_t c = sc->warp_b[w];
+    before += (w < warp) ? c : 0u;
+    tot += c;
+  }
+  __syncthreads();
+  *total = tot;
+  return before + x - v;
 }
 
 // Histogram of digit 0 of the row's keys over [start, end).
@@ -173,33 +177,68 @@ __device__ void hist_digit0(const float *srow, int start, int end, uint32_t *his
   }
 }
 
-// Pass 1 over [start, end): digit 0 > b0 (>= b0 when the whole bin b0 is
-// taken) -> candidate; digit 0 == b0 -> hist1[digit 1] (when hist1 is given).
-// Pass 2 (pass2 == true): digit 0 == b0 and digit 1 >= b1 -> candidate.
-__device__ void scan_row(const float *srow, int start, int end, bool pass2, uint32_t b0, bool whole_b0, uint32_t b1,
-                         uint32_t *hist1, const Sink &sink, Scratch *sc) {
-  for (int base = start; base < end; base += kThreads * kUnroll) {  // warp-uniform trip count
-    float v[kUnroll];
+// What the digit-0 histogram says about a row: the threshold bin b0, how many
+// of the k winners it must supply (need1) and whether pass 1 takes it whole
+// (because the k-th key's bin is exhausted exactly, or because everything at
+// or above b0 fits the select buffer).
+struct RowPlan {
+  uint32_t b0, need1;
+  bool take_b0;
+};
+
+__device__ __forceinline__ RowPlan plan_row(const uint32_t *hist0, uint32_t K, Scratch *sc) {
+  find_threshold_bin<kBins0>(hist0, K, sc);
+  RowPlan r;
+  r.b0 = sc->result[0];
+  r.need1 = sc->result[1];
+  const uint32_t bin = sc->result[2];
+  const uint32_t above = K - r.need1;
+  r.take_b0 = r.need1 == bin || above + bin <= static_cast<uint32_t>(kSmemCand);
+  __syncthreads();
+  return r;
+}
+
+// One pass over [start, end) that appends the composites of the chosen
+// elements to dst[0 ..] in position order; entries at or past `cap` are
+// counted but not written.  PASS 1 chooses digit 0 > b0 (>= b0 with
+// take_b0) and, given hist1, counts digit 1 of bin b0 into it; PASS 2 chooses
+// bin b0 at sub-bin b1 or above.  Returns the count (the same in every thread).
+template <int PASS>
+__device__ uint32_t scan_ordered(const float *srow, int start, int end, const RowPlan &rp, uint32_t b1,
+                                 uint32_t *hist1, uint64_t *dst, uint32_t cap, Scratch *sc) {
+  uint32_t count = 0;
+  for (int base = start; base < end; base += kThreads * 8) {  // block-uniform trip count
+    const int i0 = base + threadIdx.x * 8;                   // 8 consecutive elements per thread
+    uint64_t comp[8];
+    uint32_t takes = 0;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int i = base + u * kThreads + threadIdx.x;
-      v[u] = i < end ? __ldg(srow + i) : -INFINITY;
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int i = base + u * kThreads + threadIdx.x;
-      const uint32_t key = score_key(v[u]);
-      const uint32_t d0 = key >> kShift0;
-      bool take;
-      if (!pass2) {
-        take = i < end && (d0 > b0 || (whole_b0 && d0 == b0));
-        if (hist1 != nullptr && i < end && d0 == b0) atomicAdd(&hist1[(key >> kShift1) & (kBins - 1)], 1u);
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u;
+      const bool in = i < end;
+      const uint32_t key = score_key(in ? __ldg(srow + i) : 0.0f);
+      const uint32_t d0 = key >> kShift0, d1 = (key >> kShift1) & (kBins - 1);
+      bool t;
+      if (PASS == 1) {
+        t = in && (d0 > rp.b0 || (rp.take_b0 && d0 == rp.b0));
+        if (hist1 != nullptr && in && d0 == rp.b0) atomicAdd(&hist1[d1], 1u);
       } else {
-        take = i < end && d0 == b0 && ((key >> kShift1) & (kBins - 1)) >= b1;
+        t = in && d0 == rp.b0 && d1 >= b1;
       }
-      sink_append(sink, sc, take, composite(key, static_cast<uint32_t>(i)));
+      takes |= (t ? 1u : 0u) << u;
+      comp[u] = composite(key, static_cast<uint32_t>(i));
     }
+    uint32_t tot;
+    uint32_t off = count + block_exclusive_sum(__popc(takes), &tot, sc);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if ((takes >> u) & 1u) {
+        if (off < cap) dst[off] = comp[u];
+        ++off;
+      }
+    }
+    count += tot;
   }
+  return count;
 }
 
 // Exact k-th largest composite among src[0..n) (1 <= k <= n): radix passes of
@@ -317,8 +356,32 @@ __device__ __forceinline__ SmemViews smem_views(uint8_t *smem) {
   SmemViews s;
   s.cand = reinterpret_cast<uint64_t *>(smem);
   s.hist = reinterpret_cast<uint32_t *>(smem + kSmemCand * 8);
-  s.sortbuf = reinterpret_cast<int32_t *>(smem + kSmemCand * 8 + kBins * 4);
+  s.sortbuf = reinterpret_cast<int32_t *>(smem + kSmemCand * 8 + kBins0 * 4);
   return s;
+}
+
+// Writes the k positions of src[0..n) (position-ordered) whose composite is >=
+// tau to out[0..k), in order: each thread takes a contiguous run.
+__device__ void write_ordered(const uint64_t *src, uint32_t n, uint64_t tau, int32_t *out, Scratch *sc) {
+  const uint32_t per = (n + kThreads - 1) / kThreads;
+  const uint32_t r0 = threadIdx.x * per;
+  const uint32_t r1 = r0 + per < n ? r0 + per : n;
+  uint32_t mine = 0;
+  for (uint32_t i = r0; i < r1; ++i) mine += src[i] >= tau ? 1u : 0u;
+  uint32_t tot;
+  uint32_t off = block_exclusive_sum(mine, &tot, sc);
+  for (uint32_t i = r0; i < r1; ++i)
+    if (src[i] >= tau) out[off++] = composite_pos(src[i]);
+}
+
+// Step 4 on n candidates in shared memory (position-ordered when `ordered`).
+__device__ void finish_row(const uint64_t *cand, uint32_t n, int K, bool ordered, const SmemViews &s, int32_t *out,
+                           Scratch *sc) {
+  const uint64_t tau = select_threshold(cand, n, static_cast<uint32_t>(K), s.hist, sc);
+  if (ordered)
+    write_ordered(cand, n, tau, out, sc);
+  else
+    write_sorted(cand, n, tau, K, s.sortbuf, out, sc);
 }
 
 // --------------------------------------------------------------------------
@@ -336,112 +399,129 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const float *__restr
   int32_t *out = idx + (size_t)row * K;
   if (write_short_row(L, K, out)) return;
   uint32_t *hist1 = reinterpret_cast<uint32_t *>(s.sortbuf);  // the sort buffer is free until the end
-  for (int i = threadIdx.x; i < kBins; i += kThreads) {
-    s.hist[i] = 0;
-    hist1[i] = 0;
-  }
-  if (threadIdx.x == 0) sc.count = 0;
+  for (int i = threadIdx.x; i < kBins0; i += kThreads) s.hist[i] = 0;
+  for (int i = threadIdx.x; i < kBins; i += kThreads) hist1[i] = 0;
   __syncthreads();
   hist_digit0(srow, 0, L, s.hist);
   __syncthreads();
-  find_threshold_bin(s.hist, static_cast<uint32_t>(K), &sc);
-  const uint32_t b0 = sc.result[0], need1 = sc.result[1];
-  const bool whole = sc.result[1] == sc.result[2];
-  const Sink sink{s.cand, kSmemCand, nullptr, nullptr, 0};
-  scan_row(srow, 0, L, false, b0, whole, 0, whole ? nullptr : hist1, sink, &sc);
-  __syncthreads();
-  if (!whole) {
-    find_threshold_bin(hist1, need1, &sc);
-    const uint32_t b1 = sc.result[0];
-    scan_row(srow, 0, L, true, b0, false, b1, nullptr, sink, &sc);
+  const RowPlan rp = plan_row(s.hist, static_cast<uint32_t>(K), &sc);
+  uint32_t n = scan_ordered<1>(srow, 0, L, rp, 0, rp.take_b0 ? nullptr : hist1, s.cand, kSmemCand, &sc);
+  if (!rp.take_b0) {
     __syncthreads();
+    find_threshold_bin(hist1, rp.need1, &sc);
+    const uint32_t b1 = sc.result[0];
+    __syncthreads();
+    const uint32_t cap = n < static_cast<uint32_t>(kSmemCand) ? kSmemCand - n : 0u;
+    n += scan_ordered<2>(srow, 0, L, rp, b1, nullptr, s.cand + (n < kSmemCand ? n : kSmemCand), cap, &sc);
   }
-  const uint32_t n = sc.count;
   __syncthreads();
   if (n > static_cast<uint32_t>(kSmemCand)) {
     row_select_multipass(srow, L, K, out, s.hist, &sc);
     return;
   }
-  const uint64_t tau = select_threshold(s.cand, n, static_cast<uint32_t>(K), s.hist, &sc);
-  write_sorted(s.cand, n, tau, K, s.sortbuf, out, &sc);
+  finish_row(s.cand, n, K, rp.take_b0, s, out, &sc);
 }
 
 // --------------------------------------------------------------------------
-// Few long rows: (chunk, row) blocks.  ghist [rows][2][kBins] (digit 0, then
-// digit 1 within bin b0) and gcount [rows] must be zero before step 1;
-// cand [rows][T] holds the composites.
+// Few long rows: (chunk, row) blocks.  ghist [rows][kBins0 + kBins] (digit 0,
+// then digit 1 within bin b0) must be zero before step 1.  plan [rows][4]
+// holds each row's RowPlan.  cand [rows][T] holds each chunk's candidates at
+// the chunk's own offset; counts [rows][nchunk][2] how many each pass left.
 // --------------------------------------------------------------------------
 struct ChunkParams {
   const float *scores;
   const int32_t *q_pos;
   int T, K, rows, chunk, nchunk;
   uint32_t *ghist;
-  uint32_t *gcount;
+  uint32_t *plan;
+  uint32_t *counts;
   uint64_t *cand;
   int32_t *idx;
 };
 
+constexpr int kGhistStride = kBins0 + kBins;  // per-row words of ghist
+
 __global__ void __launch_bounds__(kThreads) topk_chunk_hist_kernel(const ChunkParams p) {
-  __shared__ uint32_t hist[kBins];
+  __shared__ uint32_t hist[kBins0];
   const int row = blockIdx.y, c = blockIdx.x;
   const int L = visible_length(p.q_pos, row, p.T);
   const int start = c * p.chunk;
   if (L <= p.K || start >= L) return;
   const int end = min(start + p.chunk, L);
-  for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
+  for (int i = threadIdx.x; i < kBins0; i += kThreads) hist[i] = 0;
   __syncthreads();
   hist_digit0(p.scores + (size_t)row * p.T, start, end, hist);
   __syncthreads();
-  uint32_t *g = p.ghist + (size_t)row * 2 * kBins;
-  for (int i = threadIdx.x; i < kBins; i += kThreads)
+  uint32_t *g = p.ghist + (size_t)row * kGhistStride;
+  for (int i = threadIdx.x; i < kBins0; i += kThreads)
     if (hist[i]) atomicAdd(g + i, hist[i]);
 }
 
-// PASS 1: candidates above bin b0 and the digit-1 histogram of bin b0.
-// PASS 2: candidates in bin b0 at or above sub-bin b1.
+// One block per row: the row's plan from its digit-0 histogram.
+__global__ void __launch_bounds__(kThreads) topk_plan_kernel(const ChunkParams p) {
+  __shared__ uint32_t hist[kBins0];
+  __shared__ Scratch sc;
+  const int row = blockIdx.x;
+  const int L = visible_length(p.q_pos, row, p.T);
+  if (L <= p.K) return;
+  const uint32_t *g0 = p.ghist + (size_t)row * kGhistStride;
+  for (int i = threadIdx.x; i < kBins0; i += kThreads) hist[i] = g0[i];
+  __syncthreads();
+  const RowPlan rp = plan_row(hist, static_cast<uint32_t>(p.K), &sc);
+  if (threadIdx.x == 0) {
+    uint32_t *pl = p.plan + (size_t)row * 4;
+    pl[0] = rp.b0;
+    pl[1] = rp.need1;
+    pl[2] = rp.take_b0 ? 1u : 0u;
+  }
+}
+
+__device__ __forceinline__ RowPlan load_plan(const ChunkParams &p, int row) {
+  const uint32_t *pl = p.plan + (size_t)row * 4;
+  RowPlan rp;
+  rp.b0 = pl[0];
+  rp.need1 = pl[1];
+  rp.take_b0 = pl[2] != 0;
+  return rp;
+}
+
+// PASS 1: the chunk's candidates of pass 1 (and, on a two-pass row, its
+// digit-1 histogram of bin b0).  PASS 2 (two-pass rows only): bin b0 at or
+// above sub-bin b1, after the chunk's pass-1 candidates.
 template <int PASS>
 __global__ void __launch_bounds__(kThreads) topk_chunk_scan_kernel(const ChunkParams p) {
   __shared__ uint32_t hist[kBins];
-  __shared__ uint64_t staged[kBlockCand];
   __shared__ Scratch sc;
   const int row = blockIdx.y, c = blockIdx.x;
   const int L = visible_length(p.q_pos, row, p.T);
   const int start = c * p.chunk;
   if (L <= p.K || start >= L) return;
   const int end = min(start + p.chunk, L);
-  const uint32_t *g0 = p.ghist + (size_t)row * 2 * kBins;
-  uint32_t *g1 = p.ghist + (size_t)row * 2 * kBins + kBins;
-  for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = g0[i];
-  if (threadIdx.x == 0) sc.count = 0;
-  __syncthreads();
-  find_threshold_bin(hist, static_cast<uint32_t>(p.K), &sc);
-  const uint32_t b0 = sc.result[0], need1 = sc.result[1];
-  const bool whole = sc.result[1] == sc.result[2];
-  if (PASS == 2 && whole) return;  // pass 1 already took bin b0 whole
+  uint32_t *g1 = p.ghist + (size_t)row * kGhistStride + kBins0;
+  const RowPlan rp = load_plan(p, row);
+  if (PASS == 2 && rp.take_b0) return;  // single-pass row
   uint32_t b1 = 0;
   if (PASS == 1) {
     for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
   } else {
     for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = g1[i];
     __syncthreads();
-    find_threshold_bin(hist, need1, &sc);
+    find_threshold_bin(hist, rp.need1, &sc);
     b1 = sc.result[0];
   }
   __syncthreads();
-  uint64_t *gdst = p.cand + (size_t)row * p.T;
-  const Sink sink{staged, kBlockCand, gdst, p.gcount + row, static_cast<uint32_t>(p.T)};
-  scan_row(p.scores + (size_t)row * p.T, start, end, PASS == 2, b0, whole, b1,
-           (PASS == 1 && !whole) ? hist : nullptr, sink, &sc);
-  __syncthreads();
-  // one global append for the staged candidates of this block
-  const uint32_t n = sc.count < static_cast<uint32_t>(kBlockCand) ? sc.count : static_cast<uint32_t>(kBlockCand);
-  if (threadIdx.x == 0) sc.base = n ? atomicAdd(p.gcount + row, n) : 0u;
-  if (PASS == 1 && !whole)
+  uint32_t *cnt = p.counts + ((size_t)row * p.nchunk + c) * 2;
+  const uint32_t before = PASS == 1 ? 0u : cnt[0];
+  uint64_t *dst = p.cand + (size_t)row * p.T + start + before;
+  const uint32_t cap = static_cast<uint32_t>(end - start) - before;  // never exceeded: positions are distinct
+  const uint32_t n = scan_ordered<PASS>(p.scores + (size_t)row * p.T, start, end, rp, b1,
+                                        (PASS == 1 && !rp.take_b0) ? hist : nullptr, dst, cap, &sc);
+  if (threadIdx.x == 0) cnt[PASS - 1] = n;
+  if (PASS == 1 && !rp.take_b0) {
+    __syncthreads();
     for (int i = threadIdx.x; i < kBins; i += kThreads)
       if (hist[i]) atomicAdd(g1 + i, hist[i]);
-  __syncthreads();
-  for (uint32_t i = threadIdx.x; i < n; i += kThreads)
-    if (sc.base + i < static_cast<uint32_t>(p.T)) gdst[sc.base + i] = staged[i];
+  }
 }
 
 __global__ void __launch_bounds__(kThreads) topk_chunk_select_kernel(const ChunkParams p) {
@@ -452,20 +532,34 @@ __global__ void __launch_bounds__(kThreads) topk_chunk_select_kernel(const Chunk
   const int L = visible_length(p.q_pos, row, p.T);
   int32_t *out = p.idx + (size_t)row * p.K;
   if (write_short_row(L, p.K, out)) return;
-  uint32_t n = p.gcount[row];  // <= L: each visible position is appended at most once
-  if (n > static_cast<uint32_t>(L)) {  // a corrupted counter: report it, never read past the row
-    if (threadIdx.x == 0) raise_error(kErrDeviceCheck);
-    n = static_cast<uint32_t>(L);
+  const RowPlan rp = load_plan(p, row);
+  // chunk c holds counts[c][0] (+ counts[c][1] on a two-pass row) candidates;
+  // their offsets in the gathered list are a prefix sum (nchunk <= kThreads)
+  const int nvalid = (L + p.chunk - 1) / p.chunk;
+  uint32_t *coff = reinterpret_cast<uint32_t *>(s.sortbuf);  // [kThreads] chunk offsets, then [kThreads] counts
+  uint32_t mine = 0;
+  if (static_cast<int>(threadIdx.x) < nvalid) {
+    const uint32_t *cnt = p.counts + ((size_t)row * p.nchunk + threadIdx.x) * 2;
+    mine = cnt[0] + (rp.take_b0 ? 0u : cnt[1]);
   }
-  const uint64_t *gc = p.cand + (size_t)row * p.T;
-  const uint64_t *src = gc;
-  if (n <= static_cast<uint32_t>(kSmemCand)) {
-    for (uint32_t i = threadIdx.x; i < n; i += kThreads) s.cand[i] = gc[i];
-    __syncthreads();
-    src = s.cand;
+  uint32_t n;
+  const uint32_t off = block_exclusive_sum(mine, &n, &sc);
+  coff[threadIdx.x] = off;
+  coff[kThreads + threadIdx.x] = mine;
+  __syncthreads();
+  if (n > static_cast<uint32_t>(kSmemCand)) {
+    row_select_multipass(p.scores + (size_t)row * p.T, L, p.K, out, s.hist, &sc);
+    return;
   }
-  const uint64_t tau = select_threshold(src, n, static_cast<uint32_t>(p.K), s.hist, &sc);
-  write_sorted(src, n, tau, p.K, s.sortbuf, out, &sc);
+  // one warp per chunk copies its run into place
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int c = warp; c < nvalid; c += kThreads / 32) {
+    const uint64_t *src = p.cand + (size_t)row * p.T + (size_t)c * p.chunk;
+    const uint32_t o = coff[c], m = coff[kThreads + c];
+    for (uint32_t i = lane; i < m; i += 32) s.cand[o + i] = src[i];
+  }
+  __syncthreads();
+  finish_row(s.cand, n, p.K, rp.take_b0, s, out, &sc);
 }
 
 }  // namespace topk
