@@ -377,8 +377,9 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
                 "traffic": profiled_traffic("indexer.cuh", w.name), "kernel": "indexer_scores_kernel<4>",
                 "kernel_ms": idx_ms, "algorithmic_flops": flops, "peak_source": f"{peak_src} bf16 burst"}
     else:
+        qg = 1 if Q == 1 else (2 if Q == 2 else 4)
         roof = {"bound": "hbm", "achieved": idx_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": idx_gbs / hbm_gbs,
-                "traffic": profiled_traffic("indexer.cuh", w.name), "kernel": "indexer_scores_kernel<1>",
+                "traffic": profiled_traffic("indexer.cuh", w.name), "kernel": f"indexer_scores_kernel<{qg}>",
                 "kernel_ms": idx_ms, "algorithmic_bytes": alg["indexer_keys"], "peak_source": f"{peak_src} hbm copy"}
     step_gbs = alg["total"] / (ms_per_step / 1e3) / 1e9
     step_roof = {"algorithmic_bytes": alg["total"], "achieved_gbs": step_gbs, "frac_of_measured_hbm": step_gbs / hbm_gbs,
