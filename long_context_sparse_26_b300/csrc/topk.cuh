@@ -207,15 +207,27 @@ template <int PASS>
 __device__ uint32_t scan_ordered(const float *srow, int start, int end, const RowPlan &rp, uint32_t b1,
                                  uint32_t *hist1, uint64_t *dst, uint32_t cap, Scratch *sc) {
   uint32_t count = 0;
+  // 16-byte loads when the row is 16-byte aligned (starts are multiples of 8)
+  const bool vec = (reinterpret_cast<uintptr_t>(srow + start) & 15u) == 0 && (start & 7) == 0;
   for (int base = start; base < end; base += kThreads * 8) {  // block-uniform trip count
     const int i0 = base + threadIdx.x * 8;                   // 8 consecutive elements per thread
+    float val[8];
+    if (vec && i0 + 8 <= end) {
+      const float4 a = __ldg(reinterpret_cast<const float4 *>(srow + i0));
+      const float4 c = __ldg(reinterpret_cast<const float4 *>(srow + i0 + 4));
+      val[0] = a.x; val[1] = a.y; val[2] = a.z; val[3] = a.w;
+      val[4] = c.x; val[5] = c.y; val[6] = c.z; val[7] = c.w;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) val[u] = i0 + u < end ? __ldg(srow + i0 + u) : 0.0f;
+    }
     uint64_t comp[8];
     uint32_t takes = 0;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int i = i0 + u;
       const bool in = i < end;
-      const uint32_t key = score_key(in ? __ldg(srow + i) : 0.0f);
+      const uint32_t key = score_key(val[u]);
       const uint32_t d0 = key >> kShift0, d1 = (key >> kShift1) & (kBins - 1);
       bool t;
       if (PASS == 1) {
