@@ -36,6 +36,9 @@
  *     with -1 when fewer than topk positions are visible.
  *   - The fixed shape constants (64x128 indexer, 64 heads, 576/512 dims) are
  *     compiled in; a config with other values returns DSA_ERR_UNSUPPORTED.
+ *   - A call with no query rows (B or Q, or S for MTP drafting, equal to 0 and
+ *     no size negative) has nothing to do: it returns DSA_OK at once and
+ *     reads no pointer.
  */
 #ifndef DSA_H_
 #define DSA_H_
@@ -81,7 +84,8 @@ void dsa_config_default(dsa_config_t *cfg);
 /* Workspace bytes needed by any call below on B sequences x Q query tokens
  * with context T and n_layers attention layers per call (a group: n_layers =
  * topk_freq; MTP drafting: Q = 1, n_layers = the number of draft steps).
- * Returns 0 for invalid arguments. */
+ * Returns 0 only for invalid arguments (a small nonzero size for an empty
+ * call). */
 size_t dsa_workspace_bytes(const dsa_config_t *cfg, int B, int Q, int T, int n_layers);
 
 /* Indexer scores (step a1).

@@ -112,6 +112,9 @@ dsa_status_t check_config(const dsa_config_t *c) {
   return DSA_OK;
 }
 
+// No query rows (B or Q zero, none negative): a valid call with nothing to do.
+inline bool empty_call(int B, int Q, int T) { return (B == 0 || Q == 0) && B >= 0 && Q >= 0 && T >= 0; }
+
 dsa_status_t check_sizes(int B, int Q, int T) {
   if (B <= 0 || Q <= 0 || T <= 0) return DSA_ERR_INVALID_ARG;
   const long long rows = static_cast<long long>(B) * Q;
@@ -369,6 +372,7 @@ void dsa_config_default(dsa_config_t *cfg) {
 }
 
 size_t dsa_workspace_bytes(const dsa_config_t *cfg, int B, int Q, int T, int n_layers) {
+  if (check_config(cfg) == DSA_OK && empty_call(B, Q, T) && n_layers >= 1 && n_layers <= kMaxLayers) return 256;
   if (check_config(cfg) != DSA_OK || check_sizes(B, Q, T) != DSA_OK || n_layers < 1 || n_layers > kMaxLayers)
     return 0;
   DeviceState *dev = nullptr;
@@ -380,6 +384,7 @@ dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const dsa_bf16_t *q_idx
                                 const dsa_bf16_t *k_idx, const int32_t *q_pos, int B, int Q, int T, float *scores,
                                 dsa_stream_t stream) {
   DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
   DSA_TRY(check_sizes(B, Q, T));
   if (!q_idx || !w || !k_idx || !q_pos || !scores) return DSA_ERR_INVALID_ARG;
   if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(q_pos) || !aligned16(scores))
@@ -392,6 +397,7 @@ dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const dsa_bf16_t *q_idx
 dsa_status_t dsa_topk_select(const dsa_config_t *cfg, const float *scores, const int32_t *q_pos, int B, int Q, int T,
                              int32_t *idx, void *ws, size_t ws_bytes, dsa_stream_t stream) {
   DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
   DSA_TRY(check_sizes(B, Q, T));
   if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
   if (!aligned16(scores) || !aligned16(q_pos) || !aligned16(idx) || (ws && !aligned16(ws))) return DSA_ERR_ALIGNMENT;
@@ -407,6 +413,7 @@ dsa_status_t dsa_sparse_mla_attn(const dsa_config_t *cfg, const dsa_bf16_t *q, c
                                  const int32_t *idx, int B, int Q, int T, dsa_bf16_t *out, float *lse, void *ws,
                                  size_t ws_bytes, dsa_stream_t stream) {
   DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
   DSA_TRY(check_sizes(B, Q, T));
   if (!q || !kv || !idx || !out) return DSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv) || !aligned16(idx) || !aligned16(out) || (lse && !aligned16(lse)) ||
@@ -432,6 +439,7 @@ dsa_status_t dsa_indexshare_group_forward(const dsa_config_t *cfg, const dsa_bf1
                                           dsa_bf16_t *const *out, int32_t *idx_out, void *ws, size_t ws_bytes,
                                           dsa_stream_t stream) {
   DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
   DSA_TRY(check_sizes(B, Q, T));
   if (n_layers < 1 || n_layers > kMaxLayers) return DSA_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * Q * n_layers > kMaxRowsY) return DSA_ERR_INVALID_ARG;
@@ -468,6 +476,7 @@ dsa_status_t dsa_mtp_draft_attn(const dsa_config_t *cfg, const int32_t *idx0, co
                                 dsa_stream_t stream) {
   DSA_TRY(check_config(cfg));
   if (!cfg->index_share_for_mtp) return DSA_ERR_UNSUPPORTED;
+  if (empty_call(B, S, T)) return DSA_OK;
   DSA_TRY(check_sizes(B, 1, T));
   if (S < 1 || S > kMaxLayers || static_cast<long long>(S) * B > kMaxRowsY) return DSA_ERR_INVALID_ARG;
   if (!idx0 || !q_steps || !kv || !out) return DSA_ERR_INVALID_ARG;
@@ -535,6 +544,7 @@ dsa_status_t dsa_sparse_mla_attn_noalloc(const dsa_config_t *cfg, const dsa_bf16
                                          const int32_t *idx, int B, int Q, int T, dsa_bf16_t *out, float *lse,
                                          dsa_stream_t stream) {
   DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
   DSA_TRY(check_sizes(B, Q, T));
   if (!q || !kv || !idx || !out) return DSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv) || !aligned16(idx) || !aligned16(out) || (lse && !aligned16(lse)))

@@ -93,7 +93,12 @@ PREFILL = Workload("prefill_Q4096_T131072", "prefill", B=1, Q=4096, T=131072, fi
 MTP = Workload("mtp_B64_T262144_S7", "mtp", B=64, Q=1, T=262144, first_pos=262143,
                n_layers=1, mtp_steps=MTP_STEPS, seed=500)
 
-WORKLOADS = {w.name: w for w in (TINY, DECODE_128K, DECODE_1M, PREFILL, MTP)}
+# Multi-token verification: each sequence's last accepted token plus 7 MTP
+# draft tokens, scored through one indexer pass (8 query tokens per sequence)
+# and 4 sparse layers over a 128K context.
+VERIFY = Workload("verify_B16_Q8_T131072", "decode", B=16, Q=8, T=131072, first_pos=131064, seed=600)
+
+WORKLOADS = {w.name: w for w in (TINY, DECODE_128K, DECODE_1M, PREFILL, MTP, VERIFY)}
 
 _TENSOR_IDS = {"q_idx": 1, "k_idx": 2, "w": 3, "q": 4, "kv": 5, "boost_pos": 6, "boost_dir": 7, "q_step": 8}
 

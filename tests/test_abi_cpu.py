@@ -68,7 +68,7 @@ def test_host_validation_rejects_before_launch(L):
     bad_cfg.sm_scale = -1.0
     assert _call_scores(L, bad_cfg, good) == 1
     assert _call_scores(L, cfg, [0] + good[1:]) == 1     # null pointer
-    assert _call_scores(L, cfg, good, B=0) == 1           # empty batch
+    assert _call_scores(L, cfg, good, B=-1) == 1          # negative batch
     assert _call_scores(L, cfg, good, T=-5) == 1
     assert _call_scores(L, cfg, good, B=70000) == 1       # rows beyond the launch limit
     assert _call_scores(L, cfg, [0x1008] + good[1:]) == 3  # misaligned
@@ -78,3 +78,19 @@ def test_host_validation_rejects_before_launch(L):
     cfg_nomtp.index_share_for_mtp = 0
     assert L.dsa_mtp_draft_attn(ctypes.byref(cfg_nomtp), *[ctypes.c_void_p(p) for p in good[:3]], 7, 1, 16,
                                 ctypes.c_void_p(good[4]), None, 0, None) == 2
+
+
+def test_empty_calls_are_a_no_op(L):
+    """No query rows: DSA_OK at once, with null pointers that are never read."""
+    cfg = binding.default_config()
+    n = None
+    assert L.dsa_indexer_scores(ctypes.byref(cfg), n, n, n, n, 0, 4, 16, n, n) == 0
+    assert L.dsa_indexer_scores(ctypes.byref(cfg), n, n, n, n, 3, 0, 16, n, n) == 0
+    assert L.dsa_topk_select(ctypes.byref(cfg), n, n, 0, 1, 16, n, n, 0, n) == 0
+    assert L.dsa_sparse_mla_attn(ctypes.byref(cfg), n, n, n, 0, 1, 16, n, n, n, 0, n) == 0
+    assert L.dsa_sparse_mla_attn_noalloc(ctypes.byref(cfg), n, n, n, 2, 0, 16, n, n, n) == 0
+    assert L.dsa_indexshare_group_forward(ctypes.byref(cfg), n, n, n, n, n, n, 4, 0, 1, 16, n, n, n, 0, n) == 0
+    assert L.dsa_mtp_draft_attn(ctypes.byref(cfg), n, n, n, 0, 4, 16, n, n, 0, n) == 0
+    assert L.dsa_mtp_draft_attn(ctypes.byref(cfg), n, n, n, 7, 0, 16, n, n, 0, n) == 0
+    assert binding.workspace_bytes(cfg, 0, 1, 16, 4) > 0
+    assert binding.workspace_bytes(cfg, -1, 1, 16, 4) == 0

@@ -322,6 +322,21 @@ def test_mtp_draft_small():
 
 # --------------------------------------------------------------------------- full-size workloads (sampled rows)
 
+def test_group_eight_layers_ragged():
+    """The largest group the ABI takes (8 layers), with a ragged context and
+    query positions that leave fewer than k visible keys for some rows."""
+    import dataclasses
+    w_ = dataclasses.replace(wl.TINY, name="eight_layers", B=2, Q=3, T=3001, first_pos=1000, n_layers=8, seed=777)
+    _group_check(w_)
+
+
+def test_full_verify_q8_sampled():
+    """Multi-token verification: 8 query tokens per sequence (the last accepted
+    token and 7 drafts) through one indexer pass, 4 layers, 128K context."""
+    _group_check(wl.VERIFY, rows=[(0, 0), (0, 7), (9, 3), (15, 7)])
+    torch.cuda.empty_cache()
+
+
 def test_full_decode_128k_sampled():
     _group_check(wl.DECODE_128K, rows=[(0, 0), (17, 0), (31, 0)])
     torch.cuda.empty_cache()
