@@ -295,6 +295,17 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
             dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, stream)
             dsa.topk_select(cfg, scores, inp.q_pos, idx, ws, stream)
             dsa.mtp_draft_attn(cfg, idx, inp.q_steps, inp.kv[0], out, ws, stream)
+    elif args.paged:
+        # the caches laid out in pages of args.paged rows, in a random page order
+        pools, table = wl.paginate([inp.k_idx] + inp.kv, args.paged, seed=w.seed)
+        inp.k_idx, inp.kv = None, None
+        torch.cuda.empty_cache()
+        k_pool, kv_pools = pools[0], pools[1:]
+        outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(w.n_layers)]
+
+        def step():
+            dsa.indexshare_group_forward_paged(cfg, inp.q_idx, inp.w, k_pool, inp.q_pos, inp.q, kv_pools, table, T,
+                                               outs, idx, ws, stream)
     else:
         outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(w.n_layers)]
 
@@ -351,15 +362,22 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
 
     # ---- the dominant kernel alone: indexer scores, timed with events on its stream
     kst = torch.cuda.Stream(device=dev)
+
+    def indexer_alone():
+        if args.paged and w.kind != "mtp":
+            dsa.indexer_scores_paged(cfg, inp.q_idx, inp.w, k_pool, table, inp.q_pos, scores, kst)
+        else:
+            dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, kst)
+
     with torch.cuda.stream(kst):
         for _ in range(3):
-            dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, kst)
+            indexer_alone()
     kst.synchronize()
     kev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     n_k = max(5, min(50, args.steps))
     kev[0].record(kst)
     for _ in range(n_k):
-        dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, kst)
+        indexer_alone()
     kev[1].record(kst)
     kst.synchronize()
     clocks.stop()
@@ -394,7 +412,7 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
         step_roof["frac_of_roofline_time"] = step_roof["roofline_ms"] / ms_per_step
 
     # ---- end to end through the public API with host buffers
-    e2e = None if args.no_e2e else run_e2e(args, w, cfg, inp, outs, idx, scores, ws, stream, dsa)
+    e2e = None if (args.no_e2e or args.paged) else run_e2e(args, w, cfg, inp, outs, idx, scores, ws, stream, dsa)
 
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -403,7 +421,8 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
         "config": {"workload": w.name, "B": B, "Q": Q, "T": T, "topk": w.topk,
                    "layers_per_group": w.n_layers if w.kind != "mtp" else 1,
                    "mtp_steps": w.mtp_steps or None, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (no flush needed)", "graph": "one step captured, replayed"},
+                   "l2": "inputs larger than L2 (no flush needed)", "graph": "one step captured, replayed",
+                   "kv_layout": f"paged, {args.paged}-row pages in random order" if args.paged else "contiguous"},
         "roofline": roof, "step_roofline": step_roof,
         "e2e": e2e,
         "gpu_launches": (launches_per_step or 0) * args.steps,
@@ -411,9 +430,9 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
         "clocks": clocks.summary(t_settle, t_wall1),
         "step_ms_median": statistics.median(step_ms),
     }
-    if w.name == wl.DECODE_1M.name and not args.no_variant:
+    if w.name == wl.DECODE_1M.name and not args.no_variant and not args.paged:
         res["per_layer_indexer"] = run_per_layer_variant(args, w, cfg, inp, dev, ms_per_step, dsa)
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not args.paged:
         res["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_budget)
     return res
 
@@ -591,6 +610,8 @@ def main():
     ap.add_argument("--settle", type=float, default=1.0, help="seconds of untimed load before timing (clock record)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="smaller batch (a small case for profiling)")
+    ap.add_argument("--paged", type=int, default=0, metavar="ROWS",
+                    help="lay the caches out in pages of ROWS rows (a multiple of 64) and run the paged entry points")
     ap.add_argument("--profile-kernel", choices=["indexer", "topk", "attention", "group"], default=None,
                     help="only run one entry point a few times (for ncu captures) and exit")
     args = ap.parse_args()

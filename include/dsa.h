@@ -171,6 +171,43 @@ dsa_status_t dsa_sparse_mla_attn_noalloc(const dsa_config_t *cfg, const dsa_bf16
                                          const int32_t *idx, int B, int Q, int T, dsa_bf16_t *out, float *lse,
                                          dsa_stream_t stream);
 
+/* Paged caches (the serving layout: fixed-size pages in a pool, one block
+ * table per sequence).  Position s of sequence b is held in row
+ *   block_table[b * max_pages + s / page_size] * page_size + s % page_size
+ * of a pool viewed as [num_pages * page_size, row].  page_size is a multiple
+ * of 64 (else DSA_ERR_UNSUPPORTED); max_pages * page_size >= T.  A page index
+ * outside [0, num_pages) is reported through the device error word
+ * (DSA_ERR_DEVICE_CHECK) and its rows read as zeros.  block_table is a DEVICE
+ * pointer; the struct itself is read on the host at the call. */
+typedef struct {
+  const int32_t *block_table;  /* [B, max_pages] */
+  int num_pages;
+  int page_size;
+  int max_pages;
+} dsa_pages_t;
+
+/* dsa_indexer_scores over a paged key cache k_pool [num_pages, page_size, 128]
+ * bf16; everything else as there. */
+dsa_status_t dsa_indexer_scores_paged(const dsa_config_t *cfg, const dsa_bf16_t *q_idx, const float *w,
+                                      const dsa_bf16_t *k_pool, const dsa_pages_t *pages, const int32_t *q_pos, int B,
+                                      int Q, int T, float *scores, dsa_stream_t stream);
+
+/* dsa_sparse_mla_attn over a paged latent cache kv_pool [num_pages, page_size,
+ * 576] bf16; idx holds logical positions, as there. */
+dsa_status_t dsa_sparse_mla_attn_paged(const dsa_config_t *cfg, const dsa_bf16_t *q, const dsa_bf16_t *kv_pool,
+                                       const dsa_pages_t *pages, const int32_t *idx, int B, int Q, int T,
+                                       dsa_bf16_t *out, float *lse, void *ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* dsa_indexshare_group_forward over a paged key cache k_pool and paged
+ * latent caches kv_pools[l] (all sharing one block table, as the layers of a
+ * model share their sequences' page layout). */
+dsa_status_t dsa_indexshare_group_forward_paged(const dsa_config_t *cfg, const dsa_bf16_t *q_idx, const float *w,
+                                                const dsa_bf16_t *k_pool, const int32_t *q_pos,
+                                                const dsa_bf16_t *const *q, const dsa_bf16_t *const *kv_pools,
+                                                int n_layers, const dsa_pages_t *pages, int B, int Q, int T,
+                                                dsa_bf16_t *const *out, int32_t *idx_out, void *ws, size_t ws_bytes,
+                                                dsa_stream_t stream);
+
 /* Human-readable name of a status. */
 const char *dsa_status_string(dsa_status_t status);
 

@@ -22,13 +22,19 @@ STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "D
 # every symbol include/dsa.h declares
 EXPORTS = ("dsa_config_default", "dsa_workspace_bytes", "dsa_indexer_scores", "dsa_topk_select",
            "dsa_sparse_mla_attn", "dsa_indexshare_group_forward", "dsa_mtp_draft_attn",
-           "dsa_status_string", "dsa_get_device_error", "dsa_sparse_mla_attn_noalloc")
+           "dsa_status_string", "dsa_get_device_error", "dsa_sparse_mla_attn_noalloc",
+           "dsa_indexer_scores_paged", "dsa_sparse_mla_attn_paged", "dsa_indexshare_group_forward_paged")
 
 
 class DsaConfig(ctypes.Structure):
     _fields_ = [("n_idx_heads", ctypes.c_int), ("idx_dim", ctypes.c_int), ("topk", ctypes.c_int),
                 ("topk_freq", ctypes.c_int), ("kv_lora_rank", ctypes.c_int), ("rope_dim", ctypes.c_int),
                 ("n_heads", ctypes.c_int), ("sm_scale", ctypes.c_float), ("index_share_for_mtp", ctypes.c_int)]
+
+
+class DsaPages(ctypes.Structure):
+    _fields_ = [("block_table", ctypes.c_void_p), ("num_pages", ctypes.c_int), ("page_size", ctypes.c_int),
+                ("max_pages", ctypes.c_int)]
 
 
 class DsaError(RuntimeError):
@@ -61,9 +67,16 @@ def lib() -> ctypes.CDLL:
                                                    _VP, _VP, _SZ, _VP]
         L.dsa_mtp_draft_attn.argtypes = [_CFG, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _SZ, _VP]
         L.dsa_sparse_mla_attn_noalloc.argtypes = [_CFG, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP]
+        _PG = ctypes.POINTER(DsaPages)
+        L.dsa_indexer_scores_paged.argtypes = [_CFG, _VP, _VP, _VP, _PG, _VP, _I, _I, _I, _VP, _VP]
+        L.dsa_sparse_mla_attn_paged.argtypes = [_CFG, _VP, _VP, _PG, _VP, _I, _I, _I, _VP, _VP, _VP, _SZ, _VP]
+        L.dsa_indexshare_group_forward_paged.argtypes = [_CFG, _VP, _VP, _VP, _VP, ctypes.POINTER(_VP),
+                                                         ctypes.POINTER(_VP), _I, _PG, _I, _I, _I,
+                                                         ctypes.POINTER(_VP), _VP, _VP, _SZ, _VP]
         for name in ("dsa_indexer_scores", "dsa_topk_select", "dsa_sparse_mla_attn",
                      "dsa_indexshare_group_forward", "dsa_mtp_draft_attn", "dsa_get_device_error",
-                     "dsa_sparse_mla_attn_noalloc"):
+                     "dsa_sparse_mla_attn_noalloc", "dsa_indexer_scores_paged", "dsa_sparse_mla_attn_paged",
+                     "dsa_indexshare_group_forward_paged"):
             getattr(L, name).restype = ctypes.c_int
         L.dsa_get_device_error.argtypes = [_VP]
         L.dsa_status_string.argtypes = [ctypes.c_int]
@@ -186,6 +199,63 @@ def mtp_draft_attn(cfg, idx0, q_steps, kv, out, ws=None, stream=None):
     S, B, T = q_steps.shape[0], q_steps.shape[1], kv.shape[1]
     _check(lib().dsa_mtp_draft_attn(ctypes.byref(cfg), _p(idx0), _p(q_steps), _p(kv), S, B, T, _p(out), _p(ws),
                                     0 if ws is None else ws.numel(), _s(stream)), "dsa_mtp_draft_attn")
+
+
+def pages_of(block_table: torch.Tensor, pool: torch.Tensor) -> DsaPages:
+    """Block-table description of a paged pool [num_pages, page_size, row]."""
+    _need(block_table, "block_table", torch.int32, 2)
+    return DsaPages(block_table.data_ptr(), pool.shape[0], pool.shape[1], block_table.shape[1])
+
+
+def indexer_scores_paged(cfg, q_idx, w, k_pool, block_table, q_pos, scores, stream=None):
+    """indexer_scores over a paged key cache k_pool [num_pages, page_size, 128] bf16; T = scores.shape[2]."""
+    _need(q_idx, "q_idx", torch.bfloat16, 4); _need(w, "w", torch.float32, 3)
+    _need(k_pool, "k_pool", torch.bfloat16, 3); _need(q_pos, "q_pos", torch.int32, 2)
+    _need(scores, "scores", torch.float32, 3)
+    pg = pages_of(block_table, k_pool)
+    B, Q, T = q_idx.shape[0], q_idx.shape[1], scores.shape[2]
+    _check(lib().dsa_indexer_scores_paged(ctypes.byref(cfg), _p(q_idx), _p(w), _p(k_pool), ctypes.byref(pg),
+                                          _p(q_pos), B, Q, T, _p(scores), _s(stream)), "dsa_indexer_scores_paged")
+
+
+def sparse_mla_attn_paged(cfg, q, kv_pool, block_table, idx, out, T, lse=None, ws=None, stream=None):
+    """sparse_mla_attn over a paged latent cache kv_pool [num_pages, page_size, 576] bf16 of context T."""
+    _need(q, "q", torch.bfloat16, 4); _need(kv_pool, "kv_pool", torch.bfloat16, 3)
+    _need(idx, "idx", torch.int32, 3); _need(out, "out", torch.bfloat16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    pg = pages_of(block_table, kv_pool)
+    B, Q = q.shape[0], q.shape[1]
+    _check(lib().dsa_sparse_mla_attn_paged(ctypes.byref(cfg), _p(q), _p(kv_pool), ctypes.byref(pg), _p(idx), B, Q, T,
+                                           _p(out), _p(lse), _p(ws), 0 if ws is None else ws.numel(), _s(stream)),
+           "dsa_sparse_mla_attn_paged")
+
+
+def indexshare_group_forward_paged(cfg, q_idx, w, k_pool, q_pos, qs, kv_pools, block_table, T, outs, idx_out=None,
+                                   ws=None, stream=None):
+    """indexshare_group_forward over a paged key cache and paged latent caches sharing one block table."""
+    _need(q_idx, "q_idx", torch.bfloat16, 4); _need(w, "w", torch.float32, 3)
+    _need(k_pool, "k_pool", torch.bfloat16, 3); _need(q_pos, "q_pos", torch.int32, 2)
+    n = len(qs)
+    if len(kv_pools) != n or len(outs) != n:
+        raise ValueError("qs, kv_pools and outs must have one tensor per layer")
+    for i in range(n):
+        _need(qs[i], f"q[{i}]", torch.bfloat16, 4); _need(kv_pools[i], f"kv_pool[{i}]", torch.bfloat16, 3)
+        _need(outs[i], f"out[{i}]", torch.bfloat16, 4)
+        if kv_pools[i].shape[:2] != k_pool.shape[:2]:
+            raise ValueError("every pool must have the key pool's pages")
+    if idx_out is not None:
+        _need(idx_out, "idx_out", torch.int32, 3)
+    pg = pages_of(block_table, k_pool)
+    B, Q = q_idx.shape[0], q_idx.shape[1]
+    arr = _VP * n
+    qa = arr(*[t.data_ptr() for t in qs])
+    ka = arr(*[t.data_ptr() for t in kv_pools])
+    oa = arr(*[t.data_ptr() for t in outs])
+    _check(lib().dsa_indexshare_group_forward_paged(ctypes.byref(cfg), _p(q_idx), _p(w), _p(k_pool), _p(q_pos), qa,
+                                                    ka, n, ctypes.byref(pg), B, Q, T, oa, _p(idx_out), _p(ws),
+                                                    0 if ws is None else ws.numel(), _s(stream)),
+           "dsa_indexshare_group_forward_paged")
 
 
 def get_device_error(stream=None) -> int:

@@ -112,6 +112,18 @@ dsa_status_t check_config(const dsa_config_t *c) {
   return DSA_OK;
 }
 
+// A block-table description for B sequences of context T.
+dsa_status_t check_pages(const dsa_pages_t *pg, int B, int T) {
+  if (pg == nullptr || pg->block_table == nullptr) return DSA_ERR_INVALID_ARG;
+  if (pg->page_size < 64 || pg->page_size % 64 != 0) return DSA_ERR_UNSUPPORTED;
+  if (pg->num_pages <= 0 || pg->max_pages <= 0) return DSA_ERR_INVALID_ARG;
+  if (static_cast<long long>(pg->max_pages) * pg->page_size < T) return DSA_ERR_INVALID_ARG;
+  if (static_cast<long long>(pg->num_pages) * pg->page_size >= (1LL << 31)) return DSA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * pg->max_pages >= (1LL << 31)) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(pg->block_table)) return DSA_ERR_ALIGNMENT;
+  return DSA_OK;
+}
+
 // No query rows (B or Q zero, none negative): a valid call with nothing to do.
 inline bool empty_call(int B, int Q, int T) { return (B == 0 || Q == 0) && B >= 0 && Q >= 0 && T >= 0; }
 
@@ -228,10 +240,15 @@ Layout layout(int B, int Q, int T, int n_layers, int K, int sms) {
 // digit-0 histograms into it (which must be zeroed before).
 dsa_status_t launch_indexer(const DeviceState &dev, const dsa_bf16_t *q_idx, const float *w, const dsa_bf16_t *k_idx,
                             const int32_t *q_pos, int B, int Q, int T, float *scores, cudaStream_t stream,
-                            uint32_t *ghist = nullptr) {
+                            uint32_t *ghist = nullptr, const dsa_pages_t *pages = nullptr) {
   const int QG = Q == 1 ? 1 : (Q == 2 ? 2 : 4);
   CUtensorMap tk, tq;
-  if (!make_tmap_128(&tk, k_idx, static_cast<unsigned long long>(B) * T, dsa::indexer::kTileKeys)) return DSA_ERR_CUDA;
+  if (pages != nullptr) {
+    if (!make_tmap_128(&tk, k_idx, static_cast<unsigned long long>(pages->num_pages) * pages->page_size, 64))
+      return DSA_ERR_CUDA;
+  } else if (!make_tmap_128(&tk, k_idx, static_cast<unsigned long long>(B) * T, dsa::indexer::kTileKeys)) {
+    return DSA_ERR_CUDA;
+  }
   if (!make_tmap_128(&tq, q_idx, static_cast<unsigned long long>(B) * Q * kIdxHeads, QG * kIdxHeads))
     return DSA_ERR_CUDA;
   dsa::indexer::Params p;
@@ -245,6 +262,10 @@ dsa_status_t launch_indexer(const DeviceState &dev, const dsa_bf16_t *q_idx, con
   p.ntiles = (T + dsa::indexer::kTileKeys - 1) / dsa::indexer::kTileKeys;
   p.units = static_cast<long long>(B) * p.ngroups * p.ntiles;
   p.stream_keys = p.ngroups == 1 ? 1 : 0;
+  p.block_table = pages ? pages->block_table : nullptr;
+  p.page_size = pages ? pages->page_size : 0;
+  p.max_pages = pages ? pages->max_pages : 0;
+  p.num_pages = pages ? pages->num_pages : 0;
   p.ghist = QG == 1 ? ghist : nullptr;
   const long long grid = p.units < dev.sms ? p.units : dev.sms;
   if (QG == 1)
@@ -324,7 +345,7 @@ inline int B_of(int rows, int Q) { return rows / Q; }
 dsa_status_t launch_attention(const DeviceState &dev, const Layout &L, uint8_t *ws, const dsa_bf16_t *const *q,
                               const dsa_bf16_t *const *kv, dsa_bf16_t *const *out, float *const *lse, int n_layers,
                               const int32_t *idx, int rows, int Q, int T, int K, float sm_scale,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const dsa_pages_t *pages = nullptr) {
   dsa::attn::Params p;
   std::memset(&p, 0, sizeof(p));
   for (int l = 0; l < n_layers; ++l) {
@@ -345,6 +366,12 @@ dsa_status_t launch_attention(const DeviceState &dev, const Layout &L, uint8_t *
   p.part_o = reinterpret_cast<float *>(ws + L.part_o);
   p.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
   p.scale_log2 = sm_scale * 1.4426950408889634f;
+  if (pages != nullptr) {
+    p.block_table = pages->block_table;
+    p.page_size = pages->page_size;
+    p.max_pages = pages->max_pages;
+    p.num_pages = pages->num_pages;
+  }
   return enqueue_attention(p, B_of(rows, Q), stream);
 }
 
@@ -353,6 +380,42 @@ dsa_status_t launch_attention(const DeviceState &dev, const Layout &L, uint8_t *
     const dsa_status_t s_ = (expr);   \
     if (s_ != DSA_OK) return s_;      \
   } while (0)
+
+// One IndexShare group (sizes and config already checked): the indexer and
+// top-k once, then every layer over the same index set.  `pages` (nullable)
+// describes a paged key cache and paged latent caches.
+dsa_status_t group_forward(const dsa_config_t *cfg, const dsa_bf16_t *q_idx, const float *w, const dsa_bf16_t *k_idx,
+                           const int32_t *q_pos, const dsa_bf16_t *const *q, const dsa_bf16_t *const *kv,
+                           int n_layers, int B, int Q, int T, dsa_bf16_t *const *out, int32_t *idx_out, void *ws,
+                           size_t ws_bytes, cudaStream_t st, const dsa_pages_t *pages) {
+  if (n_layers < 1 || n_layers > kMaxLayers) return DSA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * Q * n_layers > kMaxRowsY) return DSA_ERR_INVALID_ARG;
+  if (!q_idx || !w || !k_idx || !q_pos || !q || !kv || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(q_pos) || (idx_out && !aligned16(idx_out)))
+    return DSA_ERR_ALIGNMENT;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!q[l] || !kv[l] || !out[l]) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q[l]) || !aligned16(kv[l]) || !aligned16(out[l])) return DSA_ERR_ALIGNMENT;
+  }
+  if (ws == nullptr) return DSA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return DSA_ERR_ALIGNMENT;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  const Layout L = layout(B, Q, T, n_layers, cfg->topk, dev->sms);
+  if (ws_bytes < L.total) return DSA_ERR_WORKSPACE;
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  float *scores = reinterpret_cast<float *>(wsb + L.scores);
+  int32_t *idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(wsb + L.idx);
+  // IndexShare: the indexer and top-k run once for the whole group ...
+  const bool fuse_hist = Q == 1 && L.ts.nchunk > 1;
+  if (fuse_hist) DSA_TRY(clear_topk_state(L, wsb, st));
+  DSA_TRY(launch_indexer(*dev, q_idx, w, k_idx, q_pos, B, Q, T, scores, st,
+                         fuse_hist ? reinterpret_cast<uint32_t *>(wsb + L.ghist) : nullptr, pages));
+  DSA_TRY(launch_topk(L, wsb, scores, q_pos, B * Q, T, cfg->topk, idx, st, fuse_hist));
+  // ... and every layer of the group attends over the same index set.
+  return launch_attention(*dev, L, wsb, q, kv, out, nullptr, n_layers, idx, B * Q, Q, T, cfg->topk, cfg->sm_scale,
+                          st, pages);
+}
 
 }  // namespace
 
@@ -441,34 +504,8 @@ dsa_status_t dsa_indexshare_group_forward(const dsa_config_t *cfg, const dsa_bf1
   DSA_TRY(check_config(cfg));
   if (empty_call(B, Q, T)) return DSA_OK;
   DSA_TRY(check_sizes(B, Q, T));
-  if (n_layers < 1 || n_layers > kMaxLayers) return DSA_ERR_INVALID_ARG;
-  if (static_cast<long long>(B) * Q * n_layers > kMaxRowsY) return DSA_ERR_INVALID_ARG;
-  if (!q_idx || !w || !k_idx || !q_pos || !q || !kv || !out) return DSA_ERR_INVALID_ARG;
-  if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(q_pos) || (idx_out && !aligned16(idx_out)))
-    return DSA_ERR_ALIGNMENT;
-  for (int l = 0; l < n_layers; ++l) {
-    if (!q[l] || !kv[l] || !out[l]) return DSA_ERR_INVALID_ARG;
-    if (!aligned16(q[l]) || !aligned16(kv[l]) || !aligned16(out[l])) return DSA_ERR_ALIGNMENT;
-  }
-  if (ws == nullptr) return DSA_ERR_WORKSPACE;
-  if (!aligned16(ws)) return DSA_ERR_ALIGNMENT;
-  DeviceState *dev = nullptr;
-  if (!device_state(&dev)) return DSA_ERR_CUDA;
-  const Layout L = layout(B, Q, T, n_layers, cfg->topk, dev->sms);
-  if (ws_bytes < L.total) return DSA_ERR_WORKSPACE;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t *wsb = static_cast<uint8_t *>(ws);
-  float *scores = reinterpret_cast<float *>(wsb + L.scores);
-  int32_t *idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(wsb + L.idx);
-  // IndexShare: the indexer and top-k run once for the whole group ...
-  const bool fuse_hist = Q == 1 && L.ts.nchunk > 1;
-  if (fuse_hist) DSA_TRY(clear_topk_state(L, wsb, st));
-  DSA_TRY(launch_indexer(*dev, q_idx, w, k_idx, q_pos, B, Q, T, scores, st,
-                         fuse_hist ? reinterpret_cast<uint32_t *>(wsb + L.ghist) : nullptr));
-  DSA_TRY(launch_topk(L, wsb, scores, q_pos, B * Q, T, cfg->topk, idx, st, fuse_hist));
-  // ... and every layer of the group attends over the same index set.
-  return launch_attention(*dev, L, wsb, q, kv, out, nullptr, n_layers, idx, B * Q, Q, T, cfg->topk, cfg->sm_scale,
-                          st);
+  return group_forward(cfg, q_idx, w, k_idx, q_pos, q, kv, n_layers, B, Q, T, out, idx_out, ws, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 dsa_status_t dsa_mtp_draft_attn(const dsa_config_t *cfg, const int32_t *idx0, const dsa_bf16_t *q_steps,
@@ -502,6 +539,61 @@ dsa_status_t dsa_mtp_draft_attn(const dsa_config_t *cfg, const int32_t *idx0, co
                           cfg->sm_scale, reinterpret_cast<cudaStream_t>(stream));
 }
 
+
+dsa_status_t dsa_indexer_scores_paged(const dsa_config_t *cfg, const dsa_bf16_t *q_idx, const float *w,
+                                      const dsa_bf16_t *k_pool, const dsa_pages_t *pages, const int32_t *q_pos, int B,
+                                      int Q, int T, float *scores, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
+  DSA_TRY(check_sizes(B, Q, T));
+  DSA_TRY(check_pages(pages, B, T));
+  if (!q_idx || !w || !k_pool || !q_pos || !scores) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_pool) || !aligned16(q_pos) || !aligned16(scores))
+    return DSA_ERR_ALIGNMENT;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  return launch_indexer(*dev, q_idx, w, k_pool, q_pos, B, Q, T, scores, reinterpret_cast<cudaStream_t>(stream),
+                        nullptr, pages);
+}
+
+dsa_status_t dsa_sparse_mla_attn_paged(const dsa_config_t *cfg, const dsa_bf16_t *q, const dsa_bf16_t *kv_pool,
+                                       const dsa_pages_t *pages, const int32_t *idx, int B, int Q, int T,
+                                       dsa_bf16_t *out, float *lse, void *ws, size_t ws_bytes, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
+  DSA_TRY(check_sizes(B, Q, T));
+  DSA_TRY(check_pages(pages, B, T));
+  if (!q || !kv_pool || !idx || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(idx) || !aligned16(out) || (lse && !aligned16(lse)) ||
+      (ws && !aligned16(ws)))
+    return DSA_ERR_ALIGNMENT;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  const Layout L = layout(B, Q, T, 1, cfg->topk, dev->sms);
+  if (attn_shape(static_cast<long long>(B) * Q, cfg->topk, dev->sms).nsplit > 1 &&
+      (ws == nullptr || ws_bytes < L.total))
+    return DSA_ERR_WORKSPACE;
+  const dsa_bf16_t *qs[1] = {q};
+  const dsa_bf16_t *kvs[1] = {kv_pool};
+  dsa_bf16_t *outs[1] = {out};
+  float *lses[1] = {lse};
+  return launch_attention(*dev, L, static_cast<uint8_t *>(ws), qs, kvs, outs, lses, 1, idx, B * Q, Q, T, cfg->topk,
+                          cfg->sm_scale, reinterpret_cast<cudaStream_t>(stream), pages);
+}
+
+dsa_status_t dsa_indexshare_group_forward_paged(const dsa_config_t *cfg, const dsa_bf16_t *q_idx, const float *w,
+                                                const dsa_bf16_t *k_pool, const int32_t *q_pos,
+                                                const dsa_bf16_t *const *q, const dsa_bf16_t *const *kv_pools,
+                                                int n_layers, const dsa_pages_t *pages, int B, int Q, int T,
+                                                dsa_bf16_t *const *out, int32_t *idx_out, void *ws, size_t ws_bytes,
+                                                dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
+  DSA_TRY(check_sizes(B, Q, T));
+  DSA_TRY(check_pages(pages, B, T));
+  return group_forward(cfg, q_idx, w, k_pool, q_pos, q, kv_pools, n_layers, B, Q, T, out, idx_out, ws, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream), pages);
+}
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

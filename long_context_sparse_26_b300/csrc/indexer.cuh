@@ -70,6 +70,11 @@ struct Params {
   long long units;       // B * ngroups * ntiles
   int stream_keys;       // 1: every key tile is read once (evict-first in L2)
   uint32_t *ghist;       // QG == 1 only, may be null: [B][8192 + 2048], digit-0 histogram in the first 8192
+  // paged key cache (block_table null: keys are [B, T, 128] contiguous):
+  // position s of sequence b is row block_table[b][s / page_size] * page_size
+  // + s % page_size of the [pages * page_size, 128] pool; page_size % 64 == 0
+  const int32_t *block_table;  // [B, max_pages]
+  int page_size, max_pages, num_pages;
 };
 
 constexpr int kHistBins = 8192;          // digit 0 of the top-k: key bits 31..19
@@ -210,7 +215,24 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
         mbar_arrive_expect_tx(&full[stage], kABytes);
         const int yk = b * p.T + tile * kTileKeys;
         uint8_t *dst = sA + stage * kABytes;
-        if (p.stream_keys) {
+        if (p.block_table != nullptr) {
+          // two 64-row boxes per 64-dim half, each located through the block
+          // table (rows past T read page 0: the epilogue masks them; a page
+          // outside the pool reads as zeros, TMA bounds every box)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int lrow = tile * kTileKeys + 64 * r;
+            const int page = lrow / p.page_size;
+            int phys = lrow < p.T ? __ldg(p.block_table + (size_t)b * p.max_pages + page) : 0;
+            if (phys < 0 || phys >= p.num_pages) {
+              raise_error(kErrDeviceCheck);
+              phys = 0;
+            }
+            const int y = phys * p.page_size + (lrow - page * p.page_size);
+            tma_load_2d_hint(dst + r * 64 * 128, &tmap_k, 0, y, &full[stage], policy);
+            tma_load_2d_hint(dst + kHalfABytes + r * 64 * 128, &tmap_k, 64, y, &full[stage], policy);
+          }
+        } else if (p.stream_keys) {
           tma_load_2d_hint(dst, &tmap_k, 0, yk, &full[stage], policy);
           tma_load_2d_hint(dst + kHalfABytes, &tmap_k, 64, yk, &full[stage], policy);
         } else {

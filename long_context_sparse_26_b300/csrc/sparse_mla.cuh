@@ -34,6 +34,11 @@ struct Params {
   float *part_o;                        // [n_layers*rows, nsplit, 64, 512]
   float *part_ml;                       // [n_layers*rows, nsplit, 64, 2]
   float scale_log2;                     // sm_scale * log2(e)
+  // paged latent caches (block_table null: kv[l] is [B, T, 576] contiguous):
+  // position s of sequence b is row block_table[b][s / page_size] * page_size
+  // + s % page_size of kv[l] viewed as a [num_pages * page_size, 576] pool
+  const int32_t *block_table;           // [B, max_pages], shared by every layer
+  int page_size, max_pages, num_pages;
 };
 
 // Merges the splits of one (layer, row, head): O = sum_s 2^(m_s - M) O_s /

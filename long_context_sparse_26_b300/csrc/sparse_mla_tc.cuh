@@ -250,17 +250,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       q_issued = true;
     }
-    const uint8_t *kvb = reinterpret_cast<const uint8_t *>(p.kv[layer]) + (size_t)b * p.T * (kDv + 64) * 2;
+    const bool paged = p.block_table != nullptr;
+    const uint8_t *kvb = reinterpret_cast<const uint8_t *>(p.kv[layer]) + (paged ? 0 : (size_t)b * p.T * (kDv + 64) * 2);
+    // row of kvb holding position pos (-1: none); the block-table load is
+    // issued a stage before the row is used
+    auto row_of = [&](int pos) -> int {
+      if (pos < 0 || !paged) return pos;
+      const int page = pos / p.page_size;
+      const int phys = __ldg(p.block_table + (size_t)b * p.max_pages + page);
+      if (phys < 0 || phys >= p.num_pages) {
+        if (warp == 0) raise_error(kErrDeviceCheck);
+        return -1;
+      }
+      return phys * p.page_size + (pos - page * p.page_size);
+    };
     // gather stage g (g = 0, 1, ...) holds index slots 32g..32g+31 of this block
     // in ring stage g % 4; lane l holds slot l of stage g, loaded three stages ahead
     const int nstage = nblk * kWinStages;
     auto load_slot = [&](int g) -> int { return g < nstage ? slot_raw(irow, slot0 + g * kStageRows + lane, p.K) : -1; };
     int n1 = load_slot(0), n2 = load_slot(1), n3 = load_slot(2);
+    int next_row = row_of(checked_pos(n1, p.T, warp == 0));
     for (int g = 0; g < nstage; ++g) {
-      const int cur = checked_pos(n1, p.T, warp == 0);
+      const int cur = next_row;
       n1 = n2;
       n2 = n3;
       n3 = load_slot(g + 3);
+      next_row = row_of(checked_pos(n1, p.T, warp == 0));
       const int s = g % kStages;
       const uint32_t ph = static_cast<uint32_t>(g / kStages) & 1u;
       if (!warp_wait(&sm->empty[s], ph ^ 1u, abort_flag)) break;

@@ -215,3 +215,25 @@ def per_layer_indexers_of(wl: Workload, q_idx: torch.Tensor, w: torch.Tensor, k_
         ws.append(head_weights(B, Q, s, device))
         ks.append(indexer_keys(B, T, s, device))
     return qs, ws, ks
+
+
+def paginate(caches, page_size: int, seed: int, spare_pages: int = 3):
+    """Lays contiguous caches [B, T, D] (one per tensor, same B and T) out as
+    pools [num_pages, page_size, D] in a random page order, with a shared
+    block table [B, ceil(T / page_size)] int32 and a few spare pages no
+    sequence uses.  Only moves data: the pools hold the same rows."""
+    B, T = caches[0].shape[0], caches[0].shape[1]
+    device = caches[0].device
+    max_pages = (T + page_size - 1) // page_size
+    num_pages = B * max_pages + spare_pages
+    g = _gen("cpu", (seed * 7919 + page_size) & 0x7FFF_FFFF)
+    perm = torch.randperm(num_pages, generator=g)[: B * max_pages].to(torch.int32)
+    block_table = perm.view(B, max_pages).contiguous().to(device)
+    pools = []
+    for c in caches:
+        pool = torch.zeros(num_pages, page_size, *c.shape[2:], dtype=c.dtype, device=device)
+        padded = torch.zeros(B, max_pages * page_size, *c.shape[2:], dtype=c.dtype, device=device)
+        padded[:, :T] = c
+        pool[block_table.view(-1).long()] = padded.view(B * max_pages, page_size, *c.shape[2:])
+        pools.append(pool)
+    return pools, block_table

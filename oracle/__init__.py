@@ -12,4 +12,5 @@ from .dsa_oracle import (  # noqa: F401
     per_layer_indexer_forward,
     mtp_draft_attn,
     indexer_flops,
+    gather_pages,
 )

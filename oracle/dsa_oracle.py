@@ -38,6 +38,12 @@ The oracle is the plain definition of each step, written out in fp64:
   target model's cache, never to MTP-produced KV ("GLM-5.2 技术报告解读",
   section "MTP层改进"; "GLM-5.2 Explained", §2.2.1 "Index Sharing and KV Cache
   Reuse for MTP").
+* ``gather_pages``: a paged cache (fixed-size pages in a pool, one block
+  table per sequence: the page-table-managed KV cache of "GLM-5.2 Explained",
+  §3 "System Optimization for 1M-Token Context Inference", and the
+  PagedAttention deployment of §5 "Deployment Reference") read back as the
+  contiguous cache it stands for: position s of sequence b is row
+  s % page_size of page block_table[b, s // page_size].
 * ``indexer_flops``: the indexer's multiply-add count per query token, shared
   or per layer ("GLM-5.2 技术报告解读", training-strategy table: IndexShare
   removes the indexer dot products and top-k of 3 of every 4 layers).
@@ -250,3 +256,19 @@ def indexer_flops(T: int, n_layers: int, share: bool, n_heads: int = 64, head_di
     """
     per_pass = 2 * n_heads * head_dim * T
     return per_pass * (1 if share else n_layers)
+
+
+# ----------------------------------------------------------------------------
+# Paged caches
+# ----------------------------------------------------------------------------
+
+def gather_pages(pool: np.ndarray, block_table: np.ndarray, T: int) -> np.ndarray:
+    """Contiguous [B, T, D] cache of a paged pool [num_pages, page_size, D]:
+    row s of sequence b is pool[block_table[b, s // page_size], s % page_size]."""
+    page_size = pool.shape[1]
+    B = block_table.shape[0]
+    s = np.arange(T)
+    out = np.empty((B, T) + pool.shape[2:], dtype=pool.dtype)
+    for b in range(B):
+        out[b] = pool[block_table[b, s // page_size], s % page_size]
+    return out

@@ -94,3 +94,19 @@ def test_empty_calls_are_a_no_op(L):
     assert L.dsa_mtp_draft_attn(ctypes.byref(cfg), n, n, n, 7, 0, 16, n, n, 0, n) == 0
     assert binding.workspace_bytes(cfg, 0, 1, 16, 4) > 0
     assert binding.workspace_bytes(cfg, -1, 1, 16, 4) == 0
+
+
+def test_paged_validation_rejects_before_launch(L):
+    cfg = binding.default_config()
+    vp = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(6)]
+    pg = binding.DsaPages(0x7000, 10, 48, 4)           # page size not a multiple of 64
+    assert L.dsa_indexer_scores_paged(ctypes.byref(cfg), vp[0], vp[1], vp[2], ctypes.byref(pg), vp[3], 1, 1, 100,
+                                      vp[4], None) == 2
+    pg = binding.DsaPages(0x7000, 10, 64, 1)           # max_pages * page_size < T
+    assert L.dsa_indexer_scores_paged(ctypes.byref(cfg), vp[0], vp[1], vp[2], ctypes.byref(pg), vp[3], 1, 1, 100,
+                                      vp[4], None) == 1
+    pg = binding.DsaPages(0x7004, 10, 64, 4)           # misaligned block table
+    assert L.dsa_sparse_mla_attn_paged(ctypes.byref(cfg), vp[0], vp[1], ctypes.byref(pg), vp[2], 1, 1, 100, vp[3],
+                                       None, None, 0, None) == 3
+    assert L.dsa_indexer_scores_paged(ctypes.byref(cfg), vp[0], vp[1], vp[2], None, vp[3], 1, 1, 100, vp[4],
+                                      None) == 1     # no block table

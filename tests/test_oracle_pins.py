@@ -301,12 +301,29 @@ def pin_indexer_flops(o):
     assert per_layer == 4 * shared
 
 
+def pin_gather_pages(o):
+    """A pool laid out by hand: pages in reverse order plus an unused page."""
+    rng = np.random.default_rng(11)
+    B, T, D, ps = 2, 7, 3, 3                      # 3 pages per sequence, the last one partial
+    cache = rng.standard_normal((B, T, D))
+    pool = np.full((7, ps, D), np.nan)            # page 6 is never used
+    table = np.array([[5, 4, 3], [2, 1, 0]])
+    for b in range(B):
+        for s in range(T):
+            pool[table[b, s // ps], s % ps] = cache[b, s]
+    assert np.array_equal(o.gather_pages(pool, table, T), cache)
+    # hand-checked rows: sequence 1, position 4 is page 1, row 1
+    pool2 = np.arange(7 * ps * D, dtype=float).reshape(7, ps, D)
+    got = o.gather_pages(pool2, table, T)
+    assert np.array_equal(got[1, 4], pool2[1, 1]) and np.array_equal(got[0, 6], pool2[3, 0])
+
+
 PINS = [
     pin_bf16_conversion, pin_indexer_golden, pin_indexer_closed_form, pin_indexer_bruteforce,
     pin_topk_golden, pin_topk_bruteforce, pin_topk_k_covers_row, pin_attn_golden,
     pin_attn_dense_special_case, pin_attn_one_hot_and_identical, pin_attn_permutation,
     pin_group_reuses_one_index_set, pin_per_layer_variant, pin_mtp_reuse_and_kv_share,
-    pin_indexer_flops,
+    pin_indexer_flops, pin_gather_pages,
 ]
 
 
@@ -406,6 +423,16 @@ def _mut_flops_per_layer_always(T, n_layers, share, n_heads=64, head_dim=128):
     return 2 * n_heads * head_dim * T * n_layers
 
 
+def _mut_pages_row_major(pool, block_table, T):
+    page_size = pool.shape[1]
+    B = block_table.shape[0]
+    s = np.arange(T)
+    out = np.empty((B, T) + pool.shape[2:], dtype=pool.dtype)
+    for b in range(B):
+        out[b] = pool[block_table[b, s % block_table.shape[1]], s // block_table.shape[1]]
+    return out
+
+
 MUTANTS = {
     "relu_after_head_sum": ("indexer_scores_row", _mut_relu_after_sum),
     "causal_mask_excludes_self": ("indexer_scores_row", _mut_mask_excludes_self),
@@ -419,6 +446,7 @@ MUTANTS = {
     "group_reads_layer0_cache": ("indexshare_group_forward", _mut_group_layer0_cache),
     "mtp_reads_first_sequence": ("mtp_draft_attn", _mut_mtp_first_sequence),
     "indexer_never_shared": ("indexer_flops", _mut_flops_per_layer_always),
+    "pages_interleaved": ("gather_pages", _mut_pages_row_major),
 }
 
 
