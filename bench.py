@@ -52,9 +52,10 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1400.0, "fallback"
 
 
-def algorithmic_bytes(w: wl.Workload, B: int) -> dict:
-    """Indexer keys read once per group + gathered latent rows (576 bf16) per layer or draft step."""
-    key_bytes = B * w.T * wl.IDX_DIM * 2
+def algorithmic_bytes(w: wl.Workload, B: int, fp8_keys: bool = False) -> dict:
+    """Indexer keys read once per group + gathered latent rows (576 bf16) per layer or draft step.
+    FP8 keys: 128 bytes and one fp32 scale per key."""
+    key_bytes = B * w.T * (wl.IDX_DIM + 4 if fp8_keys else wl.IDX_DIM * 2)
     uses = w.mtp_steps if w.kind == "mtp" else w.n_layers
     gather = uses * B * w.Q * w.topk * wl.D_QK * 2
     return {"indexer_keys": key_bytes, "gathered_rows": gather, "total": key_bytes + gather}
@@ -295,6 +296,15 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
             dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, stream)
             dsa.topk_select(cfg, scores, inp.q_pos, idx, ws, stream)
             dsa.mtp_draft_attn(cfg, idx, inp.q_steps, inp.kv[0], out, ws, stream)
+    elif args.fp8_indexer:
+        # FP8 (E4M3) indexer caches with one fp32 scale per row; bf16 latents
+        q8, q_scale = wl.to_e4m3_rows(inp.q_idx)
+        k8, k_scale = wl.to_e4m3_rows(inp.k_idx)
+        outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(w.n_layers)]
+
+        def step():
+            dsa.indexshare_group_forward_fp8(cfg, q8, q_scale, inp.w, k8, k_scale, inp.q_pos, inp.q, inp.kv, outs,
+                                             idx, ws, stream)
     elif args.paged:
         # the caches laid out in pages of args.paged rows, in a random page order
         pools, table = wl.paginate([inp.k_idx] + inp.kv, args.paged, seed=w.seed)
@@ -364,7 +374,9 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
     kst = torch.cuda.Stream(device=dev)
 
     def indexer_alone():
-        if args.paged and w.kind != "mtp":
+        if args.fp8_indexer and w.kind != "mtp":
+            dsa.indexer_scores_fp8(cfg, q8, q_scale, inp.w, k8, k_scale, inp.q_pos, scores, kst)
+        elif args.paged and w.kind != "mtp":
             dsa.indexer_scores_paged(cfg, inp.q_idx, inp.w, k_pool, table, inp.q_pos, scores, kst)
         else:
             dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, kst)
@@ -384,7 +396,7 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
     idx_ms = kev[0].elapsed_time(kev[1]) / n_k
 
     hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = measured_peaks()
-    alg = algorithmic_bytes(w, B)
+    alg = algorithmic_bytes(w, B, fp8_keys=bool(args.fp8_indexer))
     flops = indexer_flops(w, B)
     tokens = B * Q * world if w.kind != "mtp" else B * w.mtp_steps * world
     value = tokens / (ms_per_step / 1e3)
@@ -412,17 +424,19 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
         step_roof["frac_of_roofline_time"] = step_roof["roofline_ms"] / ms_per_step
 
     # ---- end to end through the public API with host buffers
-    e2e = None if (args.no_e2e or args.paged) else run_e2e(args, w, cfg, inp, outs, idx, scores, ws, stream, dsa)
+    e2e = None if (args.no_e2e or args.paged or args.fp8_indexer) else run_e2e(args, w, cfg, inp, outs, idx, scores, ws,
+                                                                             stream, dsa)
 
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
+        "dtype": "fp8 e4m3 indexer, bf16 attention" if args.fp8_indexer else "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "Q": Q, "T": T, "topk": w.topk,
                    "layers_per_group": w.n_layers if w.kind != "mtp" else 1,
                    "mtp_steps": w.mtp_steps or None, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (no flush needed)", "graph": "one step captured, replayed",
-                   "kv_layout": f"paged, {args.paged}-row pages in random order" if args.paged else "contiguous"},
+                   "kv_layout": f"paged, {args.paged}-row pages in random order" if args.paged else "contiguous",
+                   "indexer_cache": "fp8 e4m3 + fp32 row scales" if args.fp8_indexer else "bf16"},
         "roofline": roof, "step_roofline": step_roof,
         "e2e": e2e,
         "gpu_launches": (launches_per_step or 0) * args.steps,
@@ -430,9 +444,9 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
         "clocks": clocks.summary(t_settle, t_wall1),
         "step_ms_median": statistics.median(step_ms),
     }
-    if w.name == wl.DECODE_1M.name and not args.no_variant and not args.paged:
+    if w.name == wl.DECODE_1M.name and not args.no_variant and not args.paged and not args.fp8_indexer:
         res["per_layer_indexer"] = run_per_layer_variant(args, w, cfg, inp, dev, ms_per_step, dsa)
-    if rank == 0 and not args.no_cpu_baseline and not args.paged:
+    if rank == 0 and not args.no_cpu_baseline and not args.paged and not args.fp8_indexer:
         res["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_budget)
     return res
 
@@ -610,6 +624,8 @@ def main():
     ap.add_argument("--settle", type=float, default=1.0, help="seconds of untimed load before timing (clock record)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="smaller batch (a small case for profiling)")
+    ap.add_argument("--fp8-indexer", action="store_true",
+                    help="store the indexer caches as FP8 (E4M3) rows with fp32 scales (decode workloads)")
     ap.add_argument("--paged", type=int, default=0, metavar="ROWS",
                     help="lay the caches out in pages of ROWS rows (a multiple of 64) and run the paged entry points")
     ap.add_argument("--profile-kernel", choices=["indexer", "topk", "attention", "group"], default=None,

@@ -208,6 +208,27 @@ dsa_status_t dsa_indexshare_group_forward_paged(const dsa_config_t *cfg, const d
                                                 dsa_bf16_t *const *out, int32_t *idx_out, void *ws, size_t ws_bytes,
                                                 dsa_stream_t stream);
 
+/* FP8 (E4M3) indexer caches, the "KV-cache FP8" storage of the pages: each
+ * 128-dim key row k8[b,s,:] (bytes, E4M3) stands for k8[b,s,:] * k_scale[b,s]
+ * and each query head row q8[b,t,j,:] for q8[b,t,j,:] * q_scale[b,t,j]; the
+ * scales are positive fp32 (a positive scale passes through the ReLU, so
+ * S[b,t,s] = k_scale[b,s] * sum_j w[b,t,j] q_scale[b,t,j] ReLU(q8 . k8)).
+ *   q_idx8 [B, Q, 64, 128] u8, q_scale [B, Q, 64] fp32, k_idx8 [B, T, 128] u8,
+ *   k_scale [B, T] fp32; everything else as for dsa_indexer_scores.  The
+ *   products are exact in the tensor cores (kind::f8f6f4) and summed in fp32. */
+dsa_status_t dsa_indexer_scores_fp8(const dsa_config_t *cfg, const uint8_t *q_idx8, const float *q_scale,
+                                    const float *w, const uint8_t *k_idx8, const float *k_scale, const int32_t *q_pos,
+                                    int B, int Q, int T, float *scores, dsa_stream_t stream);
+
+/* dsa_indexshare_group_forward with FP8 indexer caches (as above); the
+ * latent caches and attention stay bf16. */
+dsa_status_t dsa_indexshare_group_forward_fp8(const dsa_config_t *cfg, const uint8_t *q_idx8, const float *q_scale,
+                                              const float *w, const uint8_t *k_idx8, const float *k_scale,
+                                              const int32_t *q_pos, const dsa_bf16_t *const *q,
+                                              const dsa_bf16_t *const *kv, int n_layers, int B, int Q, int T,
+                                              dsa_bf16_t *const *out, int32_t *idx_out, void *ws, size_t ws_bytes,
+                                              dsa_stream_t stream);
+
 /* Human-readable name of a status. */
 const char *dsa_status_string(dsa_status_t status);
 

@@ -23,7 +23,8 @@ STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "D
 EXPORTS = ("dsa_config_default", "dsa_workspace_bytes", "dsa_indexer_scores", "dsa_topk_select",
            "dsa_sparse_mla_attn", "dsa_indexshare_group_forward", "dsa_mtp_draft_attn",
            "dsa_status_string", "dsa_get_device_error", "dsa_sparse_mla_attn_noalloc",
-           "dsa_indexer_scores_paged", "dsa_sparse_mla_attn_paged", "dsa_indexshare_group_forward_paged")
+           "dsa_indexer_scores_paged", "dsa_sparse_mla_attn_paged", "dsa_indexshare_group_forward_paged",
+           "dsa_indexer_scores_fp8", "dsa_indexshare_group_forward_fp8")
 
 
 class DsaConfig(ctypes.Structure):
@@ -73,10 +74,15 @@ def lib() -> ctypes.CDLL:
         L.dsa_indexshare_group_forward_paged.argtypes = [_CFG, _VP, _VP, _VP, _VP, ctypes.POINTER(_VP),
                                                          ctypes.POINTER(_VP), _I, _PG, _I, _I, _I,
                                                          ctypes.POINTER(_VP), _VP, _VP, _SZ, _VP]
+        L.dsa_indexer_scores_fp8.argtypes = [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _VP, _VP]
+        L.dsa_indexshare_group_forward_fp8.argtypes = [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(_VP),
+                                                       ctypes.POINTER(_VP), _I, _I, _I, _I, ctypes.POINTER(_VP),
+                                                       _VP, _VP, _SZ, _VP]
         for name in ("dsa_indexer_scores", "dsa_topk_select", "dsa_sparse_mla_attn",
                      "dsa_indexshare_group_forward", "dsa_mtp_draft_attn", "dsa_get_device_error",
                      "dsa_sparse_mla_attn_noalloc", "dsa_indexer_scores_paged", "dsa_sparse_mla_attn_paged",
-                     "dsa_indexshare_group_forward_paged"):
+                     "dsa_indexshare_group_forward_paged", "dsa_indexer_scores_fp8",
+                     "dsa_indexshare_group_forward_fp8"):
             getattr(L, name).restype = ctypes.c_int
         L.dsa_get_device_error.argtypes = [_VP]
         L.dsa_status_string.argtypes = [ctypes.c_int]
@@ -256,6 +262,40 @@ def indexshare_group_forward_paged(cfg, q_idx, w, k_pool, q_pos, qs, kv_pools, b
                                                     ka, n, ctypes.byref(pg), B, Q, T, oa, _p(idx_out), _p(ws),
                                                     0 if ws is None else ws.numel(), _s(stream)),
            "dsa_indexshare_group_forward_paged")
+
+
+def indexer_scores_fp8(cfg, q8, q_scale, w, k8, k_scale, q_pos, scores, stream=None):
+    """FP8 indexer caches: q8 [B,Q,64,128] u8 + q_scale [B,Q,64] f32, k8 [B,T,128] u8 + k_scale [B,T] f32."""
+    _need(q8, "q8", torch.uint8, 4); _need(q_scale, "q_scale", torch.float32, 3); _need(w, "w", torch.float32, 3)
+    _need(k8, "k8", torch.uint8, 3); _need(k_scale, "k_scale", torch.float32, 2); _need(q_pos, "q_pos", torch.int32, 2)
+    _need(scores, "scores", torch.float32, 3)
+    B, Q, T = q8.shape[0], q8.shape[1], k8.shape[1]
+    _check(lib().dsa_indexer_scores_fp8(ctypes.byref(cfg), _p(q8), _p(q_scale), _p(w), _p(k8), _p(k_scale), _p(q_pos),
+                                        B, Q, T, _p(scores), _s(stream)), "dsa_indexer_scores_fp8")
+
+
+def indexshare_group_forward_fp8(cfg, q8, q_scale, w, k8, k_scale, q_pos, qs, kvs, outs, idx_out=None, ws=None,
+                                 stream=None):
+    """One IndexShare group with FP8 indexer caches; the latent caches stay bf16."""
+    _need(q8, "q8", torch.uint8, 4); _need(q_scale, "q_scale", torch.float32, 3); _need(w, "w", torch.float32, 3)
+    _need(k8, "k8", torch.uint8, 3); _need(k_scale, "k_scale", torch.float32, 2); _need(q_pos, "q_pos", torch.int32, 2)
+    n = len(qs)
+    if len(kvs) != n or len(outs) != n:
+        raise ValueError("qs, kvs and outs must have one tensor per layer")
+    for i in range(n):
+        _need(qs[i], f"q[{i}]", torch.bfloat16, 4); _need(kvs[i], f"kv[{i}]", torch.bfloat16, 3)
+        _need(outs[i], f"out[{i}]", torch.bfloat16, 4)
+    if idx_out is not None:
+        _need(idx_out, "idx_out", torch.int32, 3)
+    B, Q, T = q8.shape[0], q8.shape[1], k8.shape[1]
+    arr = _VP * n
+    qa = arr(*[t.data_ptr() for t in qs])
+    ka = arr(*[t.data_ptr() for t in kvs])
+    oa = arr(*[t.data_ptr() for t in outs])
+    _check(lib().dsa_indexshare_group_forward_fp8(ctypes.byref(cfg), _p(q8), _p(q_scale), _p(w), _p(k8), _p(k_scale),
+                                                  _p(q_pos), qa, ka, n, B, Q, T, oa, _p(idx_out), _p(ws),
+                                                  0 if ws is None else ws.numel(), _s(stream)),
+           "dsa_indexshare_group_forward_fp8")
 
 
 def get_device_error(stream=None) -> int:

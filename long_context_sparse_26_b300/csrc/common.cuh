@@ -163,6 +163,28 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 (8-bit inputs as the
+// instruction descriptor says, fp32 accumulate); K = 32 per instruction.
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::f8f6f4: D fp32, A and B E4M3 (format code 0),
+// both K-major.
+__host__ __device__ constexpr uint32_t tc_idesc_e4m3(int M, int N) {
+  return (1u << 4)                              // D format: f32
+         | (0u << 7)                            // A format: E4M3
+         | (0u << 10)                           // B format: E4M3
+         | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
+}
+
 // The mbarrier receives one arrival once every tcgen05 operation this thread
 // issued before has completed.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {

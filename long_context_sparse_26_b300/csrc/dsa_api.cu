@@ -54,6 +54,15 @@ bool device_state(DeviceState **out) {
                                dsa::indexer::Cfg<2>::kSmemBytes) == cudaSuccess;
     ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dsa::indexer::Cfg<4>::kSmemBytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<1, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::indexer::Cfg<1, true>::kSmemBytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<2, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::indexer::Cfg<2, true>::kSmemBytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<4, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::indexer::Cfg<4, true>::kSmemBytes) == cudaSuccess;
     ok &= cudaFuncSetAttribute(dsa::mla::sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dsa::mla::kSmemBytes) == cudaSuccess;
     ok &= cudaFuncSetAttribute(dsa::topk::topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -84,6 +93,19 @@ bool make_tmap_128(CUtensorMap *map, const void *ptr, unsigned long long rows, u
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 2D tensor map over a row-major [rows, 128] matrix of E4M3 bytes, 128-byte
+// swizzle, box = the whole 128-byte row x box_rows rows.
+bool make_tmap_e4m3_128(CUtensorMap *map, const void *ptr, unsigned long long rows, unsigned box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kIdxDim)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kIdxDim), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -238,19 +260,23 @@ Layout layout(int B, int Q, int T, int n_layers, int K, int sms) {
 // ---------------------------------------------------------------------------
 // ghist: when non-null (and Q == 1), the indexer also counts the top-k's
 // digit-0 histograms into it (which must be zeroed before).
-dsa_status_t launch_indexer(const DeviceState &dev, const dsa_bf16_t *q_idx, const float *w, const dsa_bf16_t *k_idx,
+// FP8 caches: q_idx / k_idx point at E4M3 bytes and the two scale arrays
+// are given (both null for bf16).
+dsa_status_t launch_indexer(const DeviceState &dev, const void *q_idx, const float *w, const void *k_idx,
                             const int32_t *q_pos, int B, int Q, int T, float *scores, cudaStream_t stream,
-                            uint32_t *ghist = nullptr, const dsa_pages_t *pages = nullptr) {
+                            uint32_t *ghist = nullptr, const dsa_pages_t *pages = nullptr,
+                            const float *q_scale = nullptr, const float *k_scale = nullptr) {
+  const bool f8 = k_scale != nullptr;
   const int QG = Q == 1 ? 1 : (Q == 2 ? 2 : 4);
   CUtensorMap tk, tq;
+  auto tmap = f8 ? make_tmap_e4m3_128 : make_tmap_128;
   if (pages != nullptr) {
-    if (!make_tmap_128(&tk, k_idx, static_cast<unsigned long long>(pages->num_pages) * pages->page_size, 64))
+    if (!tmap(&tk, k_idx, static_cast<unsigned long long>(pages->num_pages) * pages->page_size, 64))
       return DSA_ERR_CUDA;
-  } else if (!make_tmap_128(&tk, k_idx, static_cast<unsigned long long>(B) * T, dsa::indexer::kTileKeys)) {
+  } else if (!tmap(&tk, k_idx, static_cast<unsigned long long>(B) * T, dsa::indexer::kTileKeys)) {
     return DSA_ERR_CUDA;
   }
-  if (!make_tmap_128(&tq, q_idx, static_cast<unsigned long long>(B) * Q * kIdxHeads, QG * kIdxHeads))
-    return DSA_ERR_CUDA;
+  if (!tmap(&tq, q_idx, static_cast<unsigned long long>(B) * Q * kIdxHeads, QG * kIdxHeads)) return DSA_ERR_CUDA;
   dsa::indexer::Params p;
   p.w = w;
   p.q_pos = q_pos;
@@ -266,17 +292,28 @@ dsa_status_t launch_indexer(const DeviceState &dev, const dsa_bf16_t *q_idx, con
   p.page_size = pages ? pages->page_size : 0;
   p.max_pages = pages ? pages->max_pages : 0;
   p.num_pages = pages ? pages->num_pages : 0;
+  p.k_scale = k_scale;
+  p.q_scale = q_scale;
   p.ghist = QG == 1 ? ghist : nullptr;
   const long long grid = p.units < dev.sms ? p.units : dev.sms;
-  if (QG == 1)
-    dsa::indexer::indexer_scores_kernel<1><<<static_cast<unsigned>(grid), dsa::indexer::Cfg<1>::kThreads,
-                                              dsa::indexer::Cfg<1>::kSmemBytes, stream>>>(tk, tq, p);
-  else if (QG == 2)
-    dsa::indexer::indexer_scores_kernel<2><<<static_cast<unsigned>(grid), dsa::indexer::Cfg<2>::kThreads,
-                                              dsa::indexer::Cfg<2>::kSmemBytes, stream>>>(tk, tq, p);
-  else
-    dsa::indexer::indexer_scores_kernel<4><<<static_cast<unsigned>(grid), dsa::indexer::Cfg<4>::kThreads,
-                                              dsa::indexer::Cfg<4>::kSmemBytes, stream>>>(tk, tq, p);
+  using dsa::indexer::Cfg;
+  using dsa::indexer::indexer_scores_kernel;
+  const unsigned g = static_cast<unsigned>(grid);
+  if (f8) {
+    if (QG == 1)
+      indexer_scores_kernel<1, true><<<g, Cfg<1, true>::kThreads, Cfg<1, true>::kSmemBytes, stream>>>(tk, tq, p);
+    else if (QG == 2)
+      indexer_scores_kernel<2, true><<<g, Cfg<2, true>::kThreads, Cfg<2, true>::kSmemBytes, stream>>>(tk, tq, p);
+    else
+      indexer_scores_kernel<4, true><<<g, Cfg<4, true>::kThreads, Cfg<4, true>::kSmemBytes, stream>>>(tk, tq, p);
+  } else {
+    if (QG == 1)
+      indexer_scores_kernel<1><<<g, Cfg<1>::kThreads, Cfg<1>::kSmemBytes, stream>>>(tk, tq, p);
+    else if (QG == 2)
+      indexer_scores_kernel<2><<<g, Cfg<2>::kThreads, Cfg<2>::kSmemBytes, stream>>>(tk, tq, p);
+    else
+      indexer_scores_kernel<4><<<g, Cfg<4>::kThreads, Cfg<4>::kSmemBytes, stream>>>(tk, tq, p);
+  }
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -384,10 +421,11 @@ dsa_status_t launch_attention(const DeviceState &dev, const Layout &L, uint8_t *
 // One IndexShare group (sizes and config already checked): the indexer and
 // top-k once, then every layer over the same index set.  `pages` (nullable)
 // describes a paged key cache and paged latent caches.
-dsa_status_t group_forward(const dsa_config_t *cfg, const dsa_bf16_t *q_idx, const float *w, const dsa_bf16_t *k_idx,
+dsa_status_t group_forward(const dsa_config_t *cfg, const void *q_idx, const float *w, const void *k_idx,
                            const int32_t *q_pos, const dsa_bf16_t *const *q, const dsa_bf16_t *const *kv,
                            int n_layers, int B, int Q, int T, dsa_bf16_t *const *out, int32_t *idx_out, void *ws,
-                           size_t ws_bytes, cudaStream_t st, const dsa_pages_t *pages) {
+                           size_t ws_bytes, cudaStream_t st, const dsa_pages_t *pages,
+                           const float *q_scale = nullptr, const float *k_scale = nullptr) {
   if (n_layers < 1 || n_layers > kMaxLayers) return DSA_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * Q * n_layers > kMaxRowsY) return DSA_ERR_INVALID_ARG;
   if (!q_idx || !w || !k_idx || !q_pos || !q || !kv || !out) return DSA_ERR_INVALID_ARG;
@@ -410,7 +448,8 @@ dsa_status_t group_forward(const dsa_config_t *cfg, const dsa_bf16_t *q_idx, con
   const bool fuse_hist = Q == 1 && L.ts.nchunk > 1;
   if (fuse_hist) DSA_TRY(clear_topk_state(L, wsb, st));
   DSA_TRY(launch_indexer(*dev, q_idx, w, k_idx, q_pos, B, Q, T, scores, st,
-                         fuse_hist ? reinterpret_cast<uint32_t *>(wsb + L.ghist) : nullptr, pages));
+                         fuse_hist ? reinterpret_cast<uint32_t *>(wsb + L.ghist) : nullptr, pages, q_scale,
+                         k_scale));
   DSA_TRY(launch_topk(L, wsb, scores, q_pos, B * Q, T, cfg->topk, idx, st, fuse_hist));
   // ... and every layer of the group attends over the same index set.
   return launch_attention(*dev, L, wsb, q, kv, out, nullptr, n_layers, idx, B * Q, Q, T, cfg->topk, cfg->sm_scale,
@@ -593,6 +632,37 @@ dsa_status_t dsa_indexshare_group_forward_paged(const dsa_config_t *cfg, const d
   DSA_TRY(check_pages(pages, B, T));
   return group_forward(cfg, q_idx, w, k_pool, q_pos, q, kv_pools, n_layers, B, Q, T, out, idx_out, ws, ws_bytes,
                        reinterpret_cast<cudaStream_t>(stream), pages);
+}
+
+dsa_status_t dsa_indexer_scores_fp8(const dsa_config_t *cfg, const uint8_t *q_idx8, const float *q_scale,
+                                    const float *w, const uint8_t *k_idx8, const float *k_scale, const int32_t *q_pos,
+                                    int B, int Q, int T, float *scores, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
+  DSA_TRY(check_sizes(B, Q, T));
+  if (!q_idx8 || !q_scale || !w || !k_idx8 || !k_scale || !q_pos || !scores) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx8) || !aligned16(q_scale) || !aligned16(w) || !aligned16(k_idx8) || !aligned16(k_scale) ||
+      !aligned16(q_pos) || !aligned16(scores))
+    return DSA_ERR_ALIGNMENT;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  return launch_indexer(*dev, q_idx8, w, k_idx8, q_pos, B, Q, T, scores, reinterpret_cast<cudaStream_t>(stream),
+                        nullptr, nullptr, q_scale, k_scale);
+}
+
+dsa_status_t dsa_indexshare_group_forward_fp8(const dsa_config_t *cfg, const uint8_t *q_idx8, const float *q_scale,
+                                              const float *w, const uint8_t *k_idx8, const float *k_scale,
+                                              const int32_t *q_pos, const dsa_bf16_t *const *q,
+                                              const dsa_bf16_t *const *kv, int n_layers, int B, int Q, int T,
+                                              dsa_bf16_t *const *out, int32_t *idx_out, void *ws, size_t ws_bytes,
+                                              dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
+  DSA_TRY(check_sizes(B, Q, T));
+  if (!q_scale || !k_scale) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_scale) || !aligned16(k_scale)) return DSA_ERR_ALIGNMENT;
+  return group_forward(cfg, q_idx8, w, k_idx8, q_pos, q, kv, n_layers, B, Q, T, out, idx_out, ws, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream), nullptr, q_scale, k_scale);
 }
 }  // extern "C"
 

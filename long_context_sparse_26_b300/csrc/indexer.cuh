@@ -39,15 +39,18 @@ namespace indexer {
 constexpr int kHeads = 64;
 constexpr int kDim = 128;
 constexpr int kTileKeys = 128;                     // UMMA M
-constexpr int kHalfABytes = kTileKeys * 64 * 2;    // one 64-dim half of a key tile: 16 KB
-constexpr int kABytes = 2 * kHalfABytes;           // 32 KB per stage
-
-template <int QG>
+// A key tile is 128 keys x 128 dims.  bf16: two 64-dim panels of 128-byte
+// rows (16 KB each); FP8 (E4M3): one panel, a 128-dim row being 128 bytes.
+template <int QG, bool F8 = false>
 struct Cfg {
   static constexpr int N = QG * kHeads;                 // UMMA N: 64, 128 or 256
-  static constexpr int kHalfBBytes = N * 64 * 2;
-  static constexpr int kBBytes = 2 * kHalfBBytes;
-  static constexpr int kStages = QG == 1 ? 5 : (QG == 2 ? 5 : 4);
+  static constexpr int kPanels = F8 ? 1 : 2;            // 128-byte panels per row
+  static constexpr int kPanelDims = F8 ? 128 : 64;      // dims per panel
+  static constexpr int kHalfABytes = kTileKeys * 128;   // one panel of a key tile: 16 KB
+  static constexpr int kABytes = kPanels * kHalfABytes; // per stage
+  static constexpr int kHalfBBytes = N * 128;
+  static constexpr int kBBytes = kPanels * kHalfBBytes;
+  static constexpr int kStages = F8 ? (QG == 1 ? 10 : 8) : (QG == 1 ? 5 : (QG == 2 ? 5 : 4));
   static constexpr int kEpiWarps = QG == 4 ? 8 : 4;
   static constexpr int kQPW = QG * 4 / kEpiWarps;       // queries per epilogue warp
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -56,6 +59,7 @@ struct Cfg {
   static constexpr int kTmemCols = (kAcc * N <= 256) ? 256 : 512;
   static constexpr int kSmall = 1024 + 4 * QG * kHeads * 4;  // barriers + flags, then per-warp weights
   static constexpr int kSmemBytes = 1024 + kStages * kABytes + kBBytes + kSmall + kHistBytes;
+  static constexpr int kKSteps = F8 ? kDim / 32 : kDim / 16;  // MMA instructions per tile
   static_assert(kSmemBytes <= 232448, "shared memory per block");
   static_assert(kAcc * N <= kTmemCols, "accumulators must fit the allocation");
 };
@@ -75,6 +79,10 @@ struct Params {
   // + s % page_size of the [pages * page_size, 128] pool; page_size % 64 == 0
   const int32_t *block_table;  // [B, max_pages]
   int page_size, max_pages, num_pages;
+  // FP8 caches only: row (b,s) of the key cache stands for k8 * k_scale[b*T+s]
+  // and head row (b,t,j) of the queries for q8 * q_scale[(b*Q+t)*64+j]
+  const float *k_scale;
+  const float *q_scale;
 };
 
 constexpr int kHistBins = 8192;          // digit 0 of the top-k: key bits 31..19
@@ -126,11 +134,13 @@ __device__ __forceinline__ int group_max_pos(const Params &p, int b, int q0) {
   return m;
 }
 
-template <int QG>
-__global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
+template <int QG, bool F8 = false>
+__global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
     indexer_scores_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                           const Params p) {
-  using C = Cfg<QG>;
+  using C = Cfg<QG, F8>;
+  constexpr int kHalfABytes = C::kHalfABytes;
+  constexpr int kABytes = C::kABytes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = base;                                   // [kStages][2 halves][128 rows][128 B]
@@ -206,8 +216,8 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
           if (b_loads > 0 && !mbar_wait_bounded(bfree, (b_loads - 1) & 1u, abort_flag)) break;
           mbar_arrive_expect_tx(bfull, C::kBBytes);
           const int yq = (b * p.Q + q0) * kHeads;
-          tma_load_2d(sB, &tmap_q, 0, yq, bfull);
-          tma_load_2d(sB + C::kHalfBBytes, &tmap_q, 64, yq, bfull);
+#pragma unroll
+          for (int h = 0; h < C::kPanels; ++h) tma_load_2d(sB + h * C::kHalfBBytes, &tmap_q, h * 64, yq, bfull);
           ++b_loads;
           cur_seg = seg;
         }
@@ -229,15 +239,17 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
               phys = 0;
             }
             const int y = phys * p.page_size + (lrow - page * p.page_size);
-            tma_load_2d_hint(dst + r * 64 * 128, &tmap_k, 0, y, &full[stage], policy);
-            tma_load_2d_hint(dst + kHalfABytes + r * 64 * 128, &tmap_k, 64, y, &full[stage], policy);
+#pragma unroll
+            for (int h = 0; h < C::kPanels; ++h)
+              tma_load_2d_hint(dst + h * kHalfABytes + r * 64 * 128, &tmap_k, h * 64, y, &full[stage], policy);
           }
         } else if (p.stream_keys) {
-          tma_load_2d_hint(dst, &tmap_k, 0, yk, &full[stage], policy);
-          tma_load_2d_hint(dst + kHalfABytes, &tmap_k, 64, yk, &full[stage], policy);
+#pragma unroll
+          for (int h = 0; h < C::kPanels; ++h)
+            tma_load_2d_hint(dst + h * kHalfABytes, &tmap_k, h * 64, yk, &full[stage], policy);
         } else {
-          tma_load_2d(dst, &tmap_k, 0, yk, &full[stage]);
-          tma_load_2d(dst + kHalfABytes, &tmap_k, 64, yk, &full[stage]);
+#pragma unroll
+          for (int h = 0; h < C::kPanels; ++h) tma_load_2d(dst + h * kHalfABytes, &tmap_k, h * 64, yk, &full[stage]);
         }
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -254,7 +266,7 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = tc_idesc_bf16(kTileKeys, C::N);
+      constexpr uint32_t idesc = F8 ? tc_idesc_e4m3(kTileKeys, C::N) : tc_idesc_bf16(kTileKeys, C::N);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       long long cur_seg = -1;
@@ -280,11 +292,15 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::N);
         const uint32_t a_stage = a0 + stage * kABytes;
 #pragma unroll
-        for (int kk = 0; kk < kDim / 16; ++kk) {
-          const uint32_t koff = (kk & 3) * 32u;  // K=16 step inside a 128-byte swizzled row
+        for (int kk = 0; kk < C::kKSteps; ++kk) {
+          // each K step is 32 bytes of a 128-byte swizzled row: 16 bf16 or 32 E4M3
+          const uint32_t koff = (kk & 3) * 32u;
           const uint64_t ad = tc_desc_sw128(a_stage + (kk >> 2) * kHalfABytes + koff);
           const uint64_t bd = tc_desc_sw128(b0 + (kk >> 2) * C::kHalfBBytes + koff);
-          tc_mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          if constexpr (F8)
+            tc_mma_f8(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          else
+            tc_mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
         }
         tc_commit(&empty[stage]);
         tc_commit(&tfull[acc]);
@@ -330,7 +346,10 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
         __syncwarp();  // the warp is done with the previous group's weights
         for (int i = lane; i < QPW * kHeads; i += 32) {
           const int q = q0 + qb + i / kHeads;
-          sw[i] = q < p.Q ? __ldg(p.w + ((size_t)b * p.Q + q) * kHeads + (i % kHeads)) : 0.0f;
+          const size_t wi = ((size_t)b * p.Q + q) * kHeads + (i % kHeads);
+          // FP8: the query head's scale folds into its weight (scales are
+          // positive, so they pass through the ReLU)
+          sw[i] = q < p.Q ? __ldg(p.w + wi) * (F8 ? __ldg(p.q_scale + wi) : 1.0f) : 0.0f;
         }
 #pragma unroll
         for (int i = 0; i < QPW; ++i) {
@@ -398,6 +417,7 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
             s = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
           }
         }
+        if (F8 && real && key < p.T) s *= __ldg(p.k_scale + (size_t)b * p.T + key);
         if (key < p.T) {
           float *row = p.scores + ((size_t)b * p.Q + q0 + qb + i) * (size_t)p.T;
           const bool vis = real && key <= posv[i];

@@ -237,3 +237,18 @@ def paginate(caches, page_size: int, seed: int, spare_pages: int = 3):
         pool[block_table.view(-1).long()] = padded.view(B * max_pages, page_size, *c.shape[2:])
         pools.append(pool)
     return pools, block_table
+
+
+E4M3_MAX = 448.0
+
+
+def to_e4m3_rows(x: torch.Tensor):
+    """Stores x [..., 128] as FP8 E4M3 rows with one fp32 scale per row
+    (amax / 448, 1 for an all-zero row): returns (codes uint8 [..., 128],
+    scale fp32 [...]).  A storage format for the inputs; each row stands for
+    codes * scale."""
+    xf = x.float()
+    amax = xf.abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    codes = (xf / scale.unsqueeze(-1)).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.contiguous(), scale.contiguous()

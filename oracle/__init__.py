@@ -13,4 +13,5 @@ from .dsa_oracle import (  # noqa: F401
     mtp_draft_attn,
     indexer_flops,
     gather_pages,
+    e4m3_to_f64,
 )

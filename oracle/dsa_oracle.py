@@ -44,6 +44,13 @@ The oracle is the plain definition of each step, written out in fp64:
   PagedAttention deployment of §5 "Deployment Reference") read back as the
   contiguous cache it stands for: position s of sequence b is row
   s % page_size of page block_table[b, s // page_size].
+* ``e4m3_to_f64``: exact value of FP8 E4M3 codes (the "KV-cache FP8" storage
+  of "GLM-5.2 技术报告解读", section "2. 后训练 Pipeline", and the
+  ``--kv-cache-dtype fp8`` of "GLM-5.2 Explained", §3), from the format
+  definition: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits,
+  subnormals at exponent 0, S.1111.111 is NaN and nothing is infinite.  An
+  FP8 cache row stands for its decoded values times its fp32 scale; the
+  oracle's indexer scores are those of the decoded, scaled rows.
 * ``indexer_flops``: the indexer's multiply-add count per query token, shared
   or per layer ("GLM-5.2 技术报告解读", training-strategy table: IndexShare
   removes the indexer dot products and top-k of 3 of every 4 layers).
@@ -272,3 +279,19 @@ def gather_pages(pool: np.ndarray, block_table: np.ndarray, T: int) -> np.ndarra
     for b in range(B):
         out[b] = pool[block_table[b, s // page_size], s % page_size]
     return out
+
+
+# ----------------------------------------------------------------------------
+# FP8 (E4M3) storage
+# ----------------------------------------------------------------------------
+
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Exact fp64 value of E4M3 byte codes (NaN for the two NaN codes)."""
+    c = np.asarray(codes).astype(np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    normal = sign * np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64))
+    sub = sign * np.ldexp(m / 8.0, -6)
+    v = np.where(e == 0, sub, normal)
+    return np.where((e == 15) & ((c & 0x7) == 7), np.nan, v)

@@ -318,12 +318,25 @@ def pin_gather_pages(o):
     assert np.array_equal(got[1, 4], pool2[1, 1]) and np.array_equal(got[0, 6], pool2[3, 0])
 
 
+def pin_e4m3_decoding(o):
+    """Values fixed by the E4M3 format: bias 7, 3 mantissa bits, subnormals, NaN at S.1111.111."""
+    codes = np.array([0x00, 0x38, 0x3C, 0x40, 0x7E, 0x08, 0x01, 0x07, 0xB8, 0xFE, 0x80, 0x30, 0x77])
+    want = [0.0, 1.0, 1.5, 2.0, 448.0, 2.0 ** -6, 2.0 ** -9, 7 * 2.0 ** -9, -1.0, -448.0, 0.0, 0.5, 240.0]
+    got = o.e4m3_to_f64(codes)
+    assert np.array_equal(got, np.array(want)), got
+    assert np.signbit(got[10])                   # 0x80 is -0
+    assert np.isnan(o.e4m3_to_f64(np.array([0x7F, 0xFF]))).all()
+    # every finite code is a distinct value, and ordered codes of one sign are increasing
+    pos = o.e4m3_to_f64(np.arange(0x00, 0x7F))
+    assert np.all(np.diff(pos) > 0)
+
+
 PINS = [
     pin_bf16_conversion, pin_indexer_golden, pin_indexer_closed_form, pin_indexer_bruteforce,
     pin_topk_golden, pin_topk_bruteforce, pin_topk_k_covers_row, pin_attn_golden,
     pin_attn_dense_special_case, pin_attn_one_hot_and_identical, pin_attn_permutation,
     pin_group_reuses_one_index_set, pin_per_layer_variant, pin_mtp_reuse_and_kv_share,
-    pin_indexer_flops, pin_gather_pages,
+    pin_indexer_flops, pin_gather_pages, pin_e4m3_decoding,
 ]
 
 
@@ -447,6 +460,7 @@ MUTANTS = {
     "mtp_reads_first_sequence": ("mtp_draft_attn", _mut_mtp_first_sequence),
     "indexer_never_shared": ("indexer_flops", _mut_flops_per_layer_always),
     "pages_interleaved": ("gather_pages", _mut_pages_row_major),
+    "e4m3_bias_8": ("e4m3_to_f64", lambda codes, _f=dsa_oracle.e4m3_to_f64: _f(codes) / 2.0),
 }
 
 
