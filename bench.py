@@ -403,23 +403,27 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
     idx_gbs = alg["indexer_keys"] / (idx_ms / 1e3) / 1e9
     idx_tfs = flops / (idx_ms / 1e3) / 1e12
     # the indexer is bound by its key stream or by its tensor work, whichever
-    # takes longer at peak (a few queries per sequence: keys; many: FLOPs)
-    tensor_bound = flops / (bf16_tf * 1e12) > alg["indexer_keys"] / (hbm_gbs * 1e9)
+    # takes longer at peak (a few queries per sequence: keys; many: FLOPs).
+    # FP8 operands: the measured bf16 peak times the nominal E4M3:bf16 dense
+    # ratio (4.5 / 2.25 PFLOP/s)
+    mma_tf = bf16_tf * (2.0 if args.fp8_indexer else 1.0)
+    mma_src = f"{peak_src} bf16 burst" + (" x 2 (nominal e4m3:bf16 dense ratio)" if args.fp8_indexer else "")
+    tensor_bound = flops / (mma_tf * 1e12) > alg["indexer_keys"] / (hbm_gbs * 1e9)
     if tensor_bound:
         qg = 1 if Q == 1 else (2 if Q == 2 else 4)
-        roof = {"bound": "tensor", "achieved": idx_tfs, "peak": bf16_tf, "unit": "TFLOP/s", "frac": idx_tfs / bf16_tf,
-                "traffic": profiled_traffic("indexer.cuh", w.name), "kernel": f"indexer_scores_kernel<{qg}>",
-                "kernel_ms": idx_ms, "algorithmic_flops": flops, "peak_source": f"{peak_src} bf16 burst"}
+        roof = {"bound": "tensor", "achieved": idx_tfs, "peak": mma_tf, "unit": "TFLOP/s", "frac": idx_tfs / mma_tf,
+                "traffic": profiled_traffic("indexer.cuh", w.name + (":fp8" if args.fp8_indexer else "")), "kernel": f"indexer_scores_kernel<{qg}>",
+                "kernel_ms": idx_ms, "algorithmic_flops": flops, "peak_source": mma_src}
     else:
         qg = 1 if Q == 1 else (2 if Q == 2 else 4)
         roof = {"bound": "hbm", "achieved": idx_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": idx_gbs / hbm_gbs,
-                "traffic": profiled_traffic("indexer.cuh", w.name), "kernel": f"indexer_scores_kernel<{qg}>",
+                "traffic": profiled_traffic("indexer.cuh", w.name + (":fp8" if args.fp8_indexer else "")), "kernel": f"indexer_scores_kernel<{qg}>",
                 "kernel_ms": idx_ms, "algorithmic_bytes": alg["indexer_keys"], "peak_source": f"{peak_src} hbm copy"}
     step_gbs = alg["total"] / (ms_per_step / 1e3) / 1e9
     step_roof = {"algorithmic_bytes": alg["total"], "achieved_gbs": step_gbs, "frac_of_measured_hbm": step_gbs / hbm_gbs,
                  "frac_of_nominal_8tbs": step_gbs / 8000.0, "roofline_ms": alg["total"] / (hbm_gbs * 1e9) * 1e3}
     if tensor_bound:
-        t_flops = flops / (bf16_tf * 1e12) * 1e3
+        t_flops = flops / (mma_tf * 1e12) * 1e3
         step_roof["roofline_ms"] = max(step_roof["roofline_ms"], t_flops)
         step_roof["frac_of_roofline_time"] = step_roof["roofline_ms"] / ms_per_step
 
@@ -585,8 +589,14 @@ def profile_kernel(args, w: wl.Workload):
         q_idx = wl.indexer_queries(B, Q, w.seed, dev)
         wt = wl.head_weights(B, Q, w.seed, dev)
         k_idx = wl.indexer_keys(B, T, w.seed, dev)
+        if args.fp8_indexer:
+            q8, q_scale = wl.to_e4m3_rows(q_idx)
+            k8, k_scale = wl.to_e4m3_rows(k_idx)
     if kind == "topk":
-        dsa.indexer_scores(cfg, q_idx, wt, k_idx, q_pos, scores)
+        if args.fp8_indexer:
+            dsa.indexer_scores_fp8(cfg, q8, q_scale, wt, k8, k_scale, q_pos, scores)
+        else:
+            dsa.indexer_scores(cfg, q_idx, wt, k_idx, q_pos, scores)
     if kind in ("attention", "group"):
         q = [wl.mla_queries(B, Q, w.seed, layer, dev) for layer in range(n_att)]
         kv = [wl.latent_cache(B, T, w.seed, layer, dev) for layer in range(n_att if w.kind != "mtp" else 1)]
@@ -594,7 +604,9 @@ def profile_kernel(args, w: wl.Workload):
     if kind == "attention":
         idx.copy_(torch.sort(torch.randint(0, T, (B, Q, w.topk), device=dev), dim=-1).values)
     for _ in range(args.warmup + args.steps):
-        if kind == "indexer":
+        if kind == "indexer" and args.fp8_indexer:
+            dsa.indexer_scores_fp8(cfg, q8, q_scale, wt, k8, k_scale, q_pos, scores)
+        elif kind == "indexer":
             dsa.indexer_scores(cfg, q_idx, wt, k_idx, q_pos, scores)
         elif kind == "topk":
             dsa.topk_select(cfg, scores, q_pos, idx, ws)

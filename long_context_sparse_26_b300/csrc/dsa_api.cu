@@ -285,7 +285,9 @@ dsa_status_t launch_indexer(const DeviceState &dev, const void *q_idx, const flo
   p.Q = Q;
   p.T = T;
   p.ngroups = (Q + QG - 1) / QG;
-  p.ntiles = (T + dsa::indexer::kTileKeys - 1) / dsa::indexer::kTileKeys;
+  // keys per unit of work: 256 for FP8 keys with one query per group, else 128
+  const int unit_keys = (f8 && QG == 1) ? dsa::indexer::Cfg<1, true>::kUnitKeys : dsa::indexer::kTileKeys;
+  p.ntiles = (T + unit_keys - 1) / unit_keys;
   p.units = static_cast<long long>(B) * p.ngroups * p.ntiles;
   p.stream_keys = p.ngroups == 1 ? 1 : 0;
   p.block_table = pages ? pages->block_table : nullptr;

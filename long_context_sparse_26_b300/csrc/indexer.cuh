@@ -18,16 +18,18 @@
 //              head sum, one coalesced fp32 store per key and query.  Four
 //              warps (one per TMEM lane quarter) for 1 or 2 queries per
 //              group; eight for 4 queries (two per quarter, two queries each),
-//              so that every scheduler interleaves two epilogue warps.
+//              so that every scheduler interleaves two epilogue warps; eight
+//              for one FP8 query too, whose units are two key tiles (two
+//              warps per quarter, one tile each).
 // Key tiles entirely after every query's position in the group are not
 // loaded; the epilogue writes -inf there.
 //
 // With one query per sequence (decode), the epilogue can also count each
 // visible score's top 13 key bits into a per-row histogram (the first step of
 // the top-k selection), so the count costs no extra pass over the scores:
-// the four epilogue warps share one 8192-bin shared-memory histogram and add
-// it to the global one when the block's sequence changes.  The flush is
-// fenced on both sides by an mbarrier the four warps arrive on (a bounded
+// the epilogue warps share one 8192-bin shared-memory histogram and add it
+// to the global one when the block's sequence changes.  The flush is fenced
+// on both sides by an mbarrier every epilogue warp arrives on (a bounded
 // wait, so a block that gives up never strands a warp).
 #pragma once
 
@@ -41,27 +43,40 @@ constexpr int kDim = 128;
 constexpr int kTileKeys = 128;                     // UMMA M
 // A key tile is 128 keys x 128 dims.  bf16: two 64-dim panels of 128-byte
 // rows (16 KB each); FP8 (E4M3): one panel, a 128-dim row being 128 bytes.
+// A unit of work (one pipeline stage, one accumulator slot) is kSub tiles.
 template <int QG, bool F8 = false>
 struct Cfg {
   static constexpr int N = QG * kHeads;                 // UMMA N: 64, 128 or 256
   static constexpr int kPanels = F8 ? 1 : 2;            // 128-byte panels per row
   static constexpr int kPanelDims = F8 ? 128 : 64;      // dims per panel
-  static constexpr int kHalfABytes = kTileKeys * 128;   // one panel of a key tile: 16 KB
-  static constexpr int kABytes = kPanels * kHalfABytes; // per stage
+  // FP8 decode: 256-key units, so that the single MMA-issuing thread's fixed
+  // cost per unit (two barrier waits, two commits, the loop) is paid once per
+  // 32 KB of keys, as it is for bf16; the two tiles of a unit go to two
+  // epilogue warps per lane quarter
+  static constexpr int kSub = (F8 && QG == 1) ? 2 : 1;
+  static constexpr int kUnitKeys = kSub * kTileKeys;
+  static constexpr int kPanelBytes = kUnitKeys * 128;   // one panel of a unit
+  static constexpr int kABytes = kPanels * kPanelBytes; // per stage: 32 KB
   static constexpr int kHalfBBytes = N * 128;
   static constexpr int kBBytes = kPanels * kHalfBBytes;
-  static constexpr int kStages = F8 ? (QG == 1 ? 10 : 8) : (QG == 1 ? 5 : (QG == 2 ? 5 : 4));
-  static constexpr int kEpiWarps = QG == 4 ? 8 : 4;
-  static constexpr int kQPW = QG * 4 / kEpiWarps;       // queries per epilogue warp
+  static constexpr int kStages = F8 ? (QG == 1 ? 5 : 8) : (QG == 1 ? 5 : (QG == 2 ? 5 : 4));
+  // with 4 queries the two warps of a quarter split the queries
+  static constexpr int kEpiWarps = (QG == 4 || kSub == 2) ? 8 : 4;
+  static constexpr int kQPW = QG * 4 * kSub / kEpiWarps;  // queries per epilogue warp
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kHistBytes = QG == 1 ? 8192 * 4 : 0;   // the block's digit-0 histogram
+  // FP8: each epilogue warp prefetches its keys' scales kScaleDepth units
+  // ahead with cp.async, so the load latency never sits between a tile's
+  // accumulator and its release
+  static constexpr int kScaleDepth = 8;
+  static constexpr int kScaleBytes = F8 ? kEpiWarps * kScaleDepth * 32 * 4 : 0;
   static constexpr int kAcc = QG == 4 ? 2 : 4;          // accumulator buffers in TMEM
-  static constexpr int kTmemCols = (kAcc * N <= 256) ? 256 : 512;
-  static constexpr int kSmall = 1024 + 4 * QG * kHeads * 4;  // barriers + flags, then per-warp weights
-  static constexpr int kSmemBytes = 1024 + kStages * kABytes + kBBytes + kSmall + kHistBytes;
+  static constexpr int kTmemCols = (kAcc * kSub * N <= 256) ? 256 : 512;
+  static constexpr int kSmall = 1024 + kEpiWarps * kQPW * kHeads * 4;  // barriers + flags, then per-warp weights
+  static constexpr int kSmemBytes = 1024 + kStages * kABytes + kBBytes + kSmall + kHistBytes + kScaleBytes;
   static constexpr int kKSteps = F8 ? kDim / 32 : kDim / 16;  // MMA instructions per tile
   static_assert(kSmemBytes <= 232448, "shared memory per block");
-  static_assert(kAcc * N <= kTmemCols, "accumulators must fit the allocation");
+  static_assert(kAcc * kSub * N <= kTmemCols, "accumulators must fit the allocation");
 };
 
 struct Params {
@@ -70,7 +85,7 @@ struct Params {
   float *scores;         // [B, Q, T]
   int B, Q, T;
   int ngroups;           // ceil(Q / QG)
-  int ntiles;            // ceil(T / 128)
+  int ntiles;            // ceil(T / keys per unit): units of one (sequence, query group)
   long long units;       // B * ngroups * ntiles
   int stream_keys;       // 1: every key tile is read once (evict-first in L2)
   uint32_t *ghist;       // QG == 1 only, may be null: [B][8192 + 2048], digit-0 histogram in the first 8192
@@ -89,10 +104,11 @@ constexpr int kHistBins = 8192;          // digit 0 of the top-k: key bits 31..1
 constexpr int kHistShift = 19;
 constexpr int kHistRowStride = 8192 + 2048;  // per-row words of the global histograms
 
-// Epilogue warp e's quarter of the block histogram is added to row `row` of
-// the global one and cleared, between two rounds on `bar` (four arrivals a
+// Epilogue warp e's share (1/NW) of the block histogram is added to row `row`
+// of the global one and cleared, between two rounds on `bar` (NW arrivals a
 // round: every warp is done counting before anyone flushes, and done
 // flushing before anyone counts again).  False if the block gave up.
+template <int NW>
 __device__ __forceinline__ bool flush_hist(uint32_t *hist, uint32_t *ghist, int row, int e, int lane, uint64_t *bar,
                                            uint32_t &bar_phase, volatile int *abort) {
   int ok = 1;
@@ -103,7 +119,7 @@ __device__ __forceinline__ bool flush_hist(uint32_t *hist, uint32_t *ghist, int 
   bar_phase ^= 1u;
   if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
   uint32_t *g = ghist + (size_t)row * kHistRowStride;
-  for (int i = e * (kHistBins / 4) + lane; i < (e + 1) * (kHistBins / 4); i += 32) {
+  for (int i = e * (kHistBins / NW) + lane; i < (e + 1) * (kHistBins / NW); i += 32) {
     const uint32_t c = hist[i];
     if (c) {
       atomicAdd(g + i, c);
@@ -134,17 +150,42 @@ __device__ __forceinline__ int group_max_pos(const Params &p, int b, int q0) {
   return m;
 }
 
+// Walks a block's units in order without a 64-bit division per unit: unit u
+// is key tile `tile` of query group `g` of sequence `b`, seg = b * ngroups + g.
+struct UnitCursor {
+  long long u, seg;
+  int tile, b, g;
+  __device__ __forceinline__ UnitCursor(long long u0, const Params &p) : u(u0) {
+    seg = u0 / p.ntiles;
+    tile = static_cast<int>(u0 - seg * p.ntiles);
+    b = static_cast<int>(seg / p.ngroups);
+    g = static_cast<int>(seg - (long long)b * p.ngroups);
+  }
+  __device__ __forceinline__ void next(const Params &p) {
+    ++u;
+    if (++tile == p.ntiles) {
+      tile = 0;
+      ++seg;
+      if (++g == p.ngroups) {
+        g = 0;
+        ++b;
+      }
+    }
+  }
+};
+
 template <int QG, bool F8 = false>
 __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
     indexer_scores_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                           const Params p) {
   using C = Cfg<QG, F8>;
-  constexpr int kHalfABytes = C::kHalfABytes;
+  constexpr int kPanelBytes = C::kPanelBytes;
   constexpr int kABytes = C::kABytes;
+  constexpr int kUnitKeys = C::kUnitKeys;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *sA = base;                                   // [kStages][2 halves][128 rows][128 B]
-  uint8_t *sB = base + C::kStages * kABytes;            // [2 halves][N rows][128 B]
+  uint8_t *sA = base;                                   // [kStages][panels][kUnitKeys rows][128 B]
+  uint8_t *sB = base + C::kStages * kABytes;            // [panels][N rows][128 B]
   uint8_t *small = sB + C::kBBytes;
   uint64_t *full = reinterpret_cast<uint64_t *>(small);
   uint64_t *empty = full + C::kStages;
@@ -160,6 +201,8 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
   // copy of its queries' head weights, so the warps never wait on one another.
   float *sw_all = reinterpret_cast<float *>(small + 1024);
   uint32_t *hist = reinterpret_cast<uint32_t *>(small + C::kSmall);  // QG == 1: [8192]
+  // FP8: [epilogue warps][kScaleDepth][32] key scales in flight
+  float *scale_ring = reinterpret_cast<float *>(small + C::kSmall + C::kHistBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -179,7 +222,7 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
     mbar_init(bfull, 1);
     mbar_init(bfree, 1);
     mbar_init(mma_done, 1);
-    mbar_init(hist_bar, 4);
+    mbar_init(hist_bar, C::kEpiWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -205,13 +248,11 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
       int seg_max = -1;
       uint32_t b_loads = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
-      for (long long u = u_begin; u < u_end && !*abort_flag; ++u) {
-        const long long seg = u / p.ntiles;
-        const int tile = static_cast<int>(u - seg * p.ntiles);
-        const int b = static_cast<int>(seg / p.ngroups);
-        const int q0 = static_cast<int>(seg - (long long)b * p.ngroups) * QG;
+      for (UnitCursor c(u_begin, p); c.u < u_end && !*abort_flag; c.next(p)) {
+        const long long seg = c.seg;
+        const int tile = c.tile, b = c.b, q0 = c.g * QG;
         if (seg != cur_seg) seg_max = group_max_pos<QG>(p, b, q0);
-        if (tile * kTileKeys > seg_max) continue;  // fully masked tile: no load
+        if (tile * kUnitKeys > seg_max) continue;  // fully masked unit: no load
         if (seg != cur_seg) {
           if (b_loads > 0 && !mbar_wait_bounded(bfree, (b_loads - 1) & 1u, abort_flag)) break;
           mbar_arrive_expect_tx(bfull, C::kBBytes);
@@ -223,15 +264,15 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
         }
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) break;
         mbar_arrive_expect_tx(&full[stage], kABytes);
-        const int yk = b * p.T + tile * kTileKeys;
+        const int yk = b * p.T + tile * kUnitKeys;
         uint8_t *dst = sA + stage * kABytes;
         if (p.block_table != nullptr) {
-          // two 64-row boxes per 64-dim half, each located through the block
-          // table (rows past T read page 0: the epilogue masks them; a page
-          // outside the pool reads as zeros, TMA bounds every box)
+          // 64-row boxes per panel, each located through the block table
+          // (rows past T read page 0: the epilogue masks them; a page outside
+          // the pool reads as zeros, TMA bounds every box)
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int lrow = tile * kTileKeys + 64 * r;
+          for (int r = 0; r < kUnitKeys / 64; ++r) {
+            const int lrow = tile * kUnitKeys + 64 * r;
             const int page = lrow / p.page_size;
             int phys = lrow < p.T ? __ldg(p.block_table + (size_t)b * p.max_pages + page) : 0;
             if (phys < 0 || phys >= p.num_pages) {
@@ -241,15 +282,20 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
             const int y = phys * p.page_size + (lrow - page * p.page_size);
 #pragma unroll
             for (int h = 0; h < C::kPanels; ++h)
-              tma_load_2d_hint(dst + h * kHalfABytes + r * 64 * 128, &tmap_k, h * 64, y, &full[stage], policy);
+              tma_load_2d_hint(dst + h * kPanelBytes + r * 64 * 128, &tmap_k, h * 64, y, &full[stage], policy);
           }
-        } else if (p.stream_keys) {
-#pragma unroll
-          for (int h = 0; h < C::kPanels; ++h)
-            tma_load_2d_hint(dst + h * kHalfABytes, &tmap_k, h * 64, yk, &full[stage], policy);
         } else {
+          // 128-row boxes (the tensor map's), kSub per panel
 #pragma unroll
-          for (int h = 0; h < C::kPanels; ++h) tma_load_2d(dst + h * kHalfABytes, &tmap_k, h * 64, yk, &full[stage]);
+          for (int t = 0; t < C::kSub; ++t)
+#pragma unroll
+            for (int h = 0; h < C::kPanels; ++h) {
+              uint8_t *box = dst + h * kPanelBytes + t * kTileKeys * 128;
+              if (p.stream_keys)
+                tma_load_2d_hint(box, &tmap_k, h * 64, yk + t * kTileKeys, &full[stage], policy);
+              else
+                tma_load_2d(box, &tmap_k, h * 64, yk + t * kTileKeys, &full[stage]);
+            }
         }
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -273,13 +319,11 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
       int seg_max = -1;
       uint32_t b_waits = 0;
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-      for (long long u = u_begin; u < u_end && !*abort_flag; ++u) {
-        const long long seg = u / p.ntiles;
-        const int tile = static_cast<int>(u - seg * p.ntiles);
-        const int b = static_cast<int>(seg / p.ngroups);
-        const int q0 = static_cast<int>(seg - (long long)b * p.ngroups) * QG;
+      for (UnitCursor c(u_begin, p); c.u < u_end && !*abort_flag; c.next(p)) {
+        const long long seg = c.seg;
+        const int tile = c.tile, b = c.b, q0 = c.g * QG;
         if (seg != cur_seg) seg_max = group_max_pos<QG>(p, b, q0);
-        if (tile * kTileKeys > seg_max) continue;
+        if (tile * kUnitKeys > seg_max) continue;
         if (seg != cur_seg) {
           if (b_waits > 0) tc_commit(bfree);  // previous group's operand is free once its MMAs finish
           if (!mbar_wait_bounded(bfull, b_waits & 1u, abort_flag)) break;
@@ -289,18 +333,23 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
         if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
         if (!mbar_wait_bounded(&full[stage], phase, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::N);
         const uint32_t a_stage = a0 + stage * kABytes;
 #pragma unroll
-        for (int kk = 0; kk < C::kKSteps; ++kk) {
-          // each K step is 32 bytes of a 128-byte swizzled row: 16 bf16 or 32 E4M3
-          const uint32_t koff = (kk & 3) * 32u;
-          const uint64_t ad = tc_desc_sw128(a_stage + (kk >> 2) * kHalfABytes + koff);
-          const uint64_t bd = tc_desc_sw128(b0 + (kk >> 2) * C::kHalfBBytes + koff);
-          if constexpr (F8)
-            tc_mma_f8(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
-          else
-            tc_mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        for (int t = 0; t < C::kSub; ++t) {
+          // tile t of the unit: its 128 rows into accumulator columns
+          // (acc * kSub + t) * N
+          const uint32_t d = tmem_base + static_cast<uint32_t>((acc * C::kSub + t) * C::N);
+#pragma unroll
+          for (int kk = 0; kk < C::kKSteps; ++kk) {
+            // each K step is 32 bytes of a 128-byte swizzled row: 16 bf16 or 32 E4M3
+            const uint32_t koff = (kk & 3) * 32u;
+            const uint64_t ad = tc_desc_sw128(a_stage + (kk >> 2) * kPanelBytes + t * kTileKeys * 128 + koff);
+            const uint64_t bd = tc_desc_sw128(b0 + (kk >> 2) * C::kHalfBBytes + koff);
+            if constexpr (F8)
+              tc_mma_f8(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            else
+              tc_mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          }
         }
         tc_commit(&empty[stage]);
         tc_commit(&tfull[acc]);
@@ -322,7 +371,11 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
     constexpr int QPW = C::kQPW;
     const int e = warp - 2;                        // epilogue warp index
     const int quarter = warp & 3;                  // TMEM lanes this warp may read
-    const int qb = (e >> 2) * QPW;                 // first query (within the group) of this warp
+    // the two warps of a lane quarter split a unit's tiles (kSub = 2) or
+    // the group's queries (4 queries)
+    const int sub = C::kSub > 1 ? (e >> 2) : 0;               // tile of the unit this warp reads
+    const int qb = C::kSub > 1 ? 0 : (e >> 2) * QPW;          // first query (within the group) of this warp
+    const int key_off = sub * kTileKeys + quarter * 32 + lane;  // this lane's key within a unit
     float *sw = sw_all + e * QPW * kHeads;
     const bool do_hist = QG == 1 && p.ghist != nullptr;
     uint32_t hist_phase = 0;
@@ -332,16 +385,35 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
     long long cur_seg = -1;
     int seg_max = -1;
     int posv[QPW];
+    float2 wreg[QG == 1 ? kHeads / 2 : 1];  // one query: its head weights live in registers
     int b = 0, q0 = 0;
-    for (long long u = u_begin; u < u_end; ++u) {
+    constexpr int kSD = C::kScaleDepth;
+    const uint32_t ks_slot0 = smem_u32(scale_ring + e * kSD * 32 + lane);
+    // FP8: one commit group per unit, issued kSD units ahead by a second
+    // cursor (units past the range or keys past T copy nothing; the group is
+    // still committed)
+    UnitCursor pc(u_begin, p);
+    auto prefetch_scale = [&]() {
+      if (pc.u < u_end) {
+        const int kk = pc.tile * kUnitKeys + key_off;
+        if (kk < p.T)
+          cp_async_4(ks_slot0 + static_cast<uint32_t>((pc.u - u_begin) & (kSD - 1)) * 128u,
+                     p.k_scale + (size_t)pc.b * p.T + kk);
+      }
+      cp_async_commit();
+      pc.next(p);
+    };
+    if constexpr (F8)
+      for (int d = 0; d < kSD; ++d) prefetch_scale();
+    for (UnitCursor c(u_begin, p); c.u < u_end; c.next(p)) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const long long seg = u / p.ntiles;
-      const int tile = static_cast<int>(u - seg * p.ntiles);
+      const long long u = c.u, seg = c.seg;
+      const int tile = c.tile;
       if (seg != cur_seg) {
-        if (do_hist && cur_seg >= 0 && !flush_hist(hist, p.ghist, b, e, lane, hist_bar, hist_phase, abort_flag))
+        if (do_hist && cur_seg >= 0 && !flush_hist<C::kEpiWarps>(hist, p.ghist, b, e, lane, hist_bar, hist_phase, abort_flag))
           break;
-        b = static_cast<int>(seg / p.ngroups);
-        q0 = static_cast<int>(seg - (long long)b * p.ngroups) * QG;
+        b = c.b;
+        q0 = c.g * QG;
         seg_max = group_max_pos<QG>(p, b, q0);
         __syncwarp();  // the warp is done with the previous group's weights
         for (int i = lane; i < QPW * kHeads; i += 32) {
@@ -359,10 +431,14 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
           posv[i] = pos < 0 ? -1 : (pos >= p.T ? p.T - 1 : pos);
         }
         __syncwarp();
+        if constexpr (QG == 1) {
+#pragma unroll
+          for (int j = 0; j < kHeads / 2; ++j) wreg[j] = reinterpret_cast<const float2 *>(sw)[j];
+        }
         cur_seg = seg;
       }
-      const int key = tile * kTileKeys + quarter * 32 + lane;
-      const bool real = tile * kTileKeys <= seg_max;
+      const int key = tile * kUnitKeys + key_off;
+      const bool real = tile * kUnitKeys <= seg_max;
       if (real) {
         // One lane polls; the verdict is shared so the whole warp either
         // proceeds to the warp-collective TMEM loads or leaves together.
@@ -372,32 +448,36 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
         if (!ok) break;
         tc_fence_after();
       }
+      float kscale = 1.0f;
+      if constexpr (F8) {
+        cp_async_wait<kSD - 1>();  // this unit's group has landed
+        kscale = scale_ring[(e * kSD + ((u - u_begin) & (kSD - 1))) * 32 + lane];
+      }
 #pragma unroll
       for (int i = 0; i < QPW; ++i) {
         if (q0 + qb + i >= p.Q) break;
         float s = 0.0f;
         if (real) {
           // both 32-column halves of the query's 64 heads, one wait
-          const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * C::N + (qb + i) * kHeads);
+          const uint32_t taddr =
+              tmem_base + lane_addr + static_cast<uint32_t>((acc * C::kSub + sub) * C::N + (qb + i) * kHeads);
           const float4 *w4 = reinterpret_cast<const float4 *>(sw + i * kHeads);
           if constexpr (QG == 1) {
-            // decode: each 32-column half is loaded and reduced in turn (the
-            // key stream, not this epilogue, sets the pace here)
+            // decode: each 32-column half is loaded and reduced in turn, two
+            // heads per paired FMA against the weights held in registers
+            // (the epilogue's instruction count sets the pace for FP8 keys)
             float v[32];
-            float s0 = 0.0f, s1 = 0.0f;
+            float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               tmem_ld_32x32b_x32(taddr + h * 32, v);
 #pragma unroll
               for (int j = 0; j < 32; j += 4) {
-                const float4 wv = w4[(h * 32 + j) >> 2];
-                s0 = fmaf(wv.x, fmaxf(v[j + 0], 0.0f), s0);
-                s1 = fmaf(wv.y, fmaxf(v[j + 1], 0.0f), s1);
-                s0 = fmaf(wv.z, fmaxf(v[j + 2], 0.0f), s0);
-                s1 = fmaf(wv.w, fmaxf(v[j + 3], 0.0f), s1);
+                a0 = ffma2(make_float2(fmaxf(v[j + 0], 0.0f), fmaxf(v[j + 1], 0.0f)), wreg[(h * 32 + j) >> 1], a0);
+                a1 = ffma2(make_float2(fmaxf(v[j + 2], 0.0f), fmaxf(v[j + 3], 0.0f)), wreg[((h * 32 + j) >> 1) + 1], a1);
               }
             }
-            s = s0 + s1;
+            s = (a0.x + a0.y) + (a1.x + a1.y);
           } else {
             uint32_t v0[32], v1[32];
             tmem_ld_32x32b_x32_nowait(taddr, v0);
@@ -417,7 +497,7 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
             s = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
           }
         }
-        if (F8 && real && key < p.T) s *= __ldg(p.k_scale + (size_t)b * p.T + key);
+        if (F8 && real && key < p.T) s *= kscale;
         if (key < p.T) {
           float *row = p.scores + ((size_t)b * p.Q + q0 + qb + i) * (size_t)p.T;
           const bool vis = real && key <= posv[i];
@@ -434,8 +514,11 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
           acc_phase ^= 1u;
         }
       }
+      // the slot just read is refilled (the read above has been consumed)
+      if constexpr (F8) prefetch_scale();
     }
-    if (do_hist && cur_seg >= 0 && !*abort_flag) flush_hist(hist, p.ghist, b, e, lane, hist_bar, hist_phase, abort_flag);
+    if constexpr (F8) asm volatile("cp.async.wait_all;" ::: "memory");
+    if (do_hist && cur_seg >= 0 && !*abort_flag) flush_hist<C::kEpiWarps>(hist, p.ghist, b, e, lane, hist_bar, hist_phase, abort_flag);
   }
 
   tc_fence_before();

@@ -37,7 +37,10 @@ def _decoded(codes, scale):
     return oracle.e4m3_to_f64(codes.cpu().numpy()) * scale.cpu().double().numpy()[..., None]
 
 
-@pytest.mark.parametrize("B,Q,T,first", [(2, 1, 3001, 3000), (1, 4, 2500, 2496), (1, 9, 4100, 4000)])
+# one query: 256-key units of two tiles; the cases put the position in either
+# tile of a unit, leave units past it unloaded and end T inside either tile
+@pytest.mark.parametrize("B,Q,T,first", [(2, 1, 3001, 3000), (3, 1, 5000, 1234), (2, 1, 700, 200), (1, 1, 257, 256),
+                                         (1, 1, 256, 100), (1, 4, 2500, 2496), (1, 9, 4100, 4000)])
 def test_fp8_indexer_scores(B, Q, T, first):
     cfg = dsa.default_config()
     q8, q_scale, w, k8, k_scale, pos = _fp8_inputs(B, Q, T, first, seed=T + Q)
