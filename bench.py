@@ -52,12 +52,12 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1400.0, "fallback"
 
 
-def algorithmic_bytes(w: wl.Workload, B: int, fp8_keys: bool = False) -> dict:
+def algorithmic_bytes(w: wl.Workload, B: int, fp8_keys: bool = False, fp8_kv: bool = False) -> dict:
     """Indexer keys read once per group + gathered latent rows (576 bf16) per layer or draft step.
-    FP8 keys: 128 bytes and one fp32 scale per key."""
+    FP8 keys: 128 bytes and one fp32 scale per key.  FP8 latent rows: 656 bytes."""
     key_bytes = B * w.T * (wl.IDX_DIM + 4 if fp8_keys else wl.IDX_DIM * 2)
     uses = w.mtp_steps if w.kind == "mtp" else w.n_layers
-    gather = uses * B * w.Q * w.topk * wl.D_QK * 2
+    gather = uses * B * w.Q * w.topk * (wl.FP8_LATENT_ROW_BYTES if fp8_kv else wl.D_QK * 2)
     return {"indexer_keys": key_bytes, "gathered_rows": gather, "total": key_bytes + gather}
 
 
@@ -297,14 +297,23 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
             dsa.topk_select(cfg, scores, inp.q_pos, idx, ws, stream)
             dsa.mtp_draft_attn(cfg, idx, inp.q_steps, inp.kv[0], out, ws, stream)
     elif args.fp8_indexer:
-        # FP8 (E4M3) indexer caches with one fp32 scale per row; bf16 latents
+        # FP8 (E4M3) indexer caches with one fp32 scale per row; bf16 latents,
+        # or FP8 latent rows too (--fp8-kv)
         q8, q_scale = wl.to_e4m3_rows(inp.q_idx)
         k8, k_scale = wl.to_e4m3_rows(inp.k_idx)
         outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(w.n_layers)]
+        if args.fp8_kv:
+            kv8s = [wl.to_fp8_latent(kv) for kv in inp.kv]
+            inp.kv = None
+            torch.cuda.empty_cache()
 
-        def step():
-            dsa.indexshare_group_forward_fp8(cfg, q8, q_scale, inp.w, k8, k_scale, inp.q_pos, inp.q, inp.kv, outs,
-                                             idx, ws, stream)
+            def step():
+                dsa.indexshare_group_forward_fp8kv(cfg, q8, q_scale, inp.w, k8, k_scale, inp.q_pos, inp.q, kv8s,
+                                                   outs, idx, ws, stream)
+        else:
+            def step():
+                dsa.indexshare_group_forward_fp8(cfg, q8, q_scale, inp.w, k8, k_scale, inp.q_pos, inp.q, inp.kv,
+                                                 outs, idx, ws, stream)
     elif args.paged:
         # the caches laid out in pages of args.paged rows, in a random page order
         pools, table = wl.paginate([inp.k_idx] + inp.kv, args.paged, seed=w.seed)
@@ -396,7 +405,7 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
     idx_ms = kev[0].elapsed_time(kev[1]) / n_k
 
     hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = measured_peaks()
-    alg = algorithmic_bytes(w, B, fp8_keys=bool(args.fp8_indexer))
+    alg = algorithmic_bytes(w, B, fp8_keys=bool(args.fp8_indexer), fp8_kv=bool(args.fp8_kv))
     flops = indexer_flops(w, B)
     tokens = B * Q * world if w.kind != "mtp" else B * w.mtp_steps * world
     value = tokens / (ms_per_step / 1e3)
@@ -434,13 +443,15 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8 e4m3 indexer, bf16 attention" if args.fp8_indexer else "bf16", "data": "synthetic",
+        "dtype": ("fp8 e4m3 indexer and latent caches, bf16 attention math" if args.fp8_kv else
+                  "fp8 e4m3 indexer, bf16 attention") if args.fp8_indexer else "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "Q": Q, "T": T, "topk": w.topk,
                    "layers_per_group": w.n_layers if w.kind != "mtp" else 1,
                    "mtp_steps": w.mtp_steps or None, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (no flush needed)", "graph": "one step captured, replayed",
                    "kv_layout": f"paged, {args.paged}-row pages in random order" if args.paged else "contiguous",
-                   "indexer_cache": "fp8 e4m3 + fp32 row scales" if args.fp8_indexer else "bf16"},
+                   "indexer_cache": "fp8 e4m3 + fp32 row scales" if args.fp8_indexer else "bf16",
+                   "latent_cache": "fp8 e4m3 + fp32 group scales, bf16 rope (656 B rows)" if args.fp8_kv else "bf16"},
         "roofline": roof, "step_roofline": step_roof,
         "e2e": e2e,
         "gpu_launches": (launches_per_step or 0) * args.steps,
@@ -600,6 +611,9 @@ def profile_kernel(args, w: wl.Workload):
     if kind in ("attention", "group"):
         q = [wl.mla_queries(B, Q, w.seed, layer, dev) for layer in range(n_att)]
         kv = [wl.latent_cache(B, T, w.seed, layer, dev) for layer in range(n_att if w.kind != "mtp" else 1)]
+        if args.fp8_kv:
+            kv = [wl.to_fp8_latent(t) for t in kv]
+            torch.cuda.empty_cache()
         outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=dev) for _ in range(n_att)]
     if kind == "attention":
         idx.copy_(torch.sort(torch.randint(0, T, (B, Q, w.topk), device=dev), dim=-1).values)
@@ -612,7 +626,8 @@ def profile_kernel(args, w: wl.Workload):
             dsa.topk_select(cfg, scores, q_pos, idx, ws)
         elif kind == "attention":
             for layer in range(n_att):
-                dsa.sparse_mla_attn(cfg, q[layer], kv[min(layer, len(kv) - 1)], idx, outs[layer], None, ws)
+                attn = dsa.sparse_mla_attn_fp8 if args.fp8_kv else dsa.sparse_mla_attn
+                attn(cfg, q[layer], kv[min(layer, len(kv) - 1)], idx, outs[layer], None, ws)
         else:
             dsa.indexshare_group_forward(cfg, q_idx, wt, k_idx, q_pos, q, kv, outs, idx, ws)
     torch.cuda.synchronize()
@@ -638,6 +653,8 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="smaller batch (a small case for profiling)")
     ap.add_argument("--fp8-indexer", action="store_true",
                     help="store the indexer caches as FP8 (E4M3) rows with fp32 scales (decode workloads)")
+    ap.add_argument("--fp8-kv", action="store_true",
+                    help="with --fp8-indexer: store the latent caches as FP8 rows too (656 bytes per position)")
     ap.add_argument("--paged", type=int, default=0, metavar="ROWS",
                     help="lay the caches out in pages of ROWS rows (a multiple of 64) and run the paged entry points")
     ap.add_argument("--profile-kernel", choices=["indexer", "topk", "attention", "group"], default=None,
@@ -645,6 +662,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.fp8_kv and not args.fp8_indexer and args.profile_kernel != "attention":
+        ap.error("--fp8-kv runs with --fp8-indexer (the all-FP8 cache entry point)")
     w = wl.WORKLOADS[args.workload]
     if args.batch is not None:
         import dataclasses

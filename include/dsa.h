@@ -229,6 +229,32 @@ dsa_status_t dsa_indexshare_group_forward_fp8(const dsa_config_t *cfg, const uin
                                               dsa_bf16_t *const *out, int32_t *idx_out, void *ws, size_t ws_bytes,
                                               dsa_stream_t stream);
 
+/* FP8 latent cache (the KV cache in FP8: "GLM-5.2 Explained: 1M Token Context
+ * AI Agent Model", §3 and §5, Deployment Reference; the pages fix no row
+ * format, so this is the library's reading, the one serving stacks use for
+ * MLA caches).  Each cached position is one 656-byte row:
+ *   bytes   0..511  the 512 compressed-KV dims as E4M3 codes,
+ *   bytes 512..527  four fp32 scales, one per 128-dim group of those codes,
+ *   bytes 528..655  the 64 RoPE dims, bf16 (kept at full width).
+ * Row (b, s) stands for dims d < 512: code[d] * scale[d / 128], dims 512..575:
+ * the RoPE values.  The kernel rounds each dequantised value to bf16 before
+ * its bf16 tensor-core products (within the attention tolerance).  Code 0x7F /
+ * 0xFF (E4M3 NaN) must not occur.
+ * dsa_sparse_mla_attn with kv8 [B, T, 656] bytes (16-byte aligned); everything
+ * else as there. */
+dsa_status_t dsa_sparse_mla_attn_fp8(const dsa_config_t *cfg, const dsa_bf16_t *q, const uint8_t *kv8,
+                                     const int32_t *idx, int B, int Q, int T, dsa_bf16_t *out, float *lse, void *ws,
+                                     size_t ws_bytes, dsa_stream_t stream);
+
+/* dsa_indexshare_group_forward_fp8 with FP8 latent caches too: kv8[l] is
+ * [B, T, 656] bytes in the row format above. */
+dsa_status_t dsa_indexshare_group_forward_fp8kv(const dsa_config_t *cfg, const uint8_t *q_idx8,
+                                                const float *q_scale, const float *w, const uint8_t *k_idx8,
+                                                const float *k_scale, const int32_t *q_pos, const dsa_bf16_t *const *q,
+                                                const uint8_t *const *kv8, int n_layers, int B, int Q, int T,
+                                                dsa_bf16_t *const *out, int32_t *idx_out, void *ws, size_t ws_bytes,
+                                                dsa_stream_t stream);
+
 /* Human-readable name of a status. */
 const char *dsa_status_string(dsa_status_t status);
 

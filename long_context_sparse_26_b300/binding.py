@@ -24,7 +24,10 @@ EXPORTS = ("dsa_config_default", "dsa_workspace_bytes", "dsa_indexer_scores", "d
            "dsa_sparse_mla_attn", "dsa_indexshare_group_forward", "dsa_mtp_draft_attn",
            "dsa_status_string", "dsa_get_device_error", "dsa_sparse_mla_attn_noalloc",
            "dsa_indexer_scores_paged", "dsa_sparse_mla_attn_paged", "dsa_indexshare_group_forward_paged",
-           "dsa_indexer_scores_fp8", "dsa_indexshare_group_forward_fp8")
+           "dsa_indexer_scores_fp8", "dsa_indexshare_group_forward_fp8", "dsa_sparse_mla_attn_fp8",
+           "dsa_indexshare_group_forward_fp8kv")
+
+FP8_LATENT_ROW_BYTES = 656  # 512 E4M3 codes, 4 fp32 group scales, 64 bf16 RoPE dims
 
 
 class DsaConfig(ctypes.Structure):
@@ -78,11 +81,16 @@ def lib() -> ctypes.CDLL:
         L.dsa_indexshare_group_forward_fp8.argtypes = [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(_VP),
                                                        ctypes.POINTER(_VP), _I, _I, _I, _I, ctypes.POINTER(_VP),
                                                        _VP, _VP, _SZ, _VP]
+        L.dsa_sparse_mla_attn_fp8.argtypes = [_CFG, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP, _SZ, _VP]
+        L.dsa_indexshare_group_forward_fp8kv.argtypes = [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(_VP),
+                                                         ctypes.POINTER(_VP), _I, _I, _I, _I, ctypes.POINTER(_VP),
+                                                         _VP, _VP, _SZ, _VP]
         for name in ("dsa_indexer_scores", "dsa_topk_select", "dsa_sparse_mla_attn",
                      "dsa_indexshare_group_forward", "dsa_mtp_draft_attn", "dsa_get_device_error",
                      "dsa_sparse_mla_attn_noalloc", "dsa_indexer_scores_paged", "dsa_sparse_mla_attn_paged",
                      "dsa_indexshare_group_forward_paged", "dsa_indexer_scores_fp8",
-                     "dsa_indexshare_group_forward_fp8"):
+                     "dsa_indexshare_group_forward_fp8", "dsa_sparse_mla_attn_fp8",
+                     "dsa_indexshare_group_forward_fp8kv"):
             getattr(L, name).restype = ctypes.c_int
         L.dsa_get_device_error.argtypes = [_VP]
         L.dsa_status_string.argtypes = [ctypes.c_int]
@@ -309,3 +317,44 @@ def status_string(status: int) -> str:
 
 def sm_scale() -> float:
     return 1.0 / math.sqrt(576)
+
+
+def _need_fp8_latent(t, name):
+    _need(t, name, torch.uint8, 3)
+    if t.shape[2] != FP8_LATENT_ROW_BYTES:
+        raise ValueError(f"{name}: FP8 latent rows are {FP8_LATENT_ROW_BYTES} bytes, got {t.shape[2]}")
+
+
+def sparse_mla_attn_fp8(cfg, q, kv8, idx, out, lse=None, ws=None, stream=None):
+    """q [B,Q,64,576] bf16, kv8 [B,T,656] u8 (FP8 latent rows), idx [B,Q,topk] i32 -> out [B,Q,64,512] bf16."""
+    _need(q, "q", torch.bfloat16, 4); _need_fp8_latent(kv8, "kv8"); _need(idx, "idx", torch.int32, 3)
+    _need(out, "out", torch.bfloat16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    B, Q, T = q.shape[0], q.shape[1], kv8.shape[1]
+    _check(lib().dsa_sparse_mla_attn_fp8(ctypes.byref(cfg), _p(q), _p(kv8), _p(idx), B, Q, T, _p(out), _p(lse),
+                                         _p(ws), 0 if ws is None else ws.numel(), _s(stream)), "dsa_sparse_mla_attn_fp8")
+
+
+def indexshare_group_forward_fp8kv(cfg, q8, q_scale, w, k8, k_scale, q_pos, qs, kv8s, outs, idx_out=None, ws=None,
+                                   stream=None):
+    """One IndexShare group with FP8 indexer caches and FP8 latent caches kv8s[l] [B,T,656] u8."""
+    _need(q8, "q8", torch.uint8, 4); _need(q_scale, "q_scale", torch.float32, 3); _need(w, "w", torch.float32, 3)
+    _need(k8, "k8", torch.uint8, 3); _need(k_scale, "k_scale", torch.float32, 2); _need(q_pos, "q_pos", torch.int32, 2)
+    n = len(qs)
+    if len(kv8s) != n or len(outs) != n:
+        raise ValueError("qs, kv8s and outs must have one tensor per layer")
+    for i in range(n):
+        _need(qs[i], f"q[{i}]", torch.bfloat16, 4); _need_fp8_latent(kv8s[i], f"kv8[{i}]")
+        _need(outs[i], f"out[{i}]", torch.bfloat16, 4)
+    if idx_out is not None:
+        _need(idx_out, "idx_out", torch.int32, 3)
+    B, Q, T = q8.shape[0], q8.shape[1], k8.shape[1]
+    arr = _VP * n
+    qa = arr(*[t.data_ptr() for t in qs])
+    ka = arr(*[t.data_ptr() for t in kv8s])
+    oa = arr(*[t.data_ptr() for t in outs])
+    _check(lib().dsa_indexshare_group_forward_fp8kv(ctypes.byref(cfg), _p(q8), _p(q_scale), _p(w), _p(k8),
+                                                    _p(k_scale), _p(q_pos), qa, ka, n, B, Q, T, oa, _p(idx_out),
+                                                    _p(ws), 0 if ws is None else ws.numel(), _s(stream)),
+           "dsa_indexshare_group_forward_fp8kv")

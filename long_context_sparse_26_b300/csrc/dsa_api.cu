@@ -63,7 +63,9 @@ bool device_state(DeviceState **out) {
     ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<4, true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dsa::indexer::Cfg<4, true>::kSmemBytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(dsa::mla::sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    ok &= cudaFuncSetAttribute(dsa::mla::sparse_mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::mla::kSmemBytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::mla::sparse_mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dsa::mla::kSmemBytes) == cudaSuccess;
     ok &= cudaFuncSetAttribute(dsa::topk::topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dsa::topk::kSelectSmem) == cudaSuccess;
@@ -369,8 +371,12 @@ dsa_status_t enqueue_attention(const dsa::attn::Params &p, int B, cudaStream_t s
     if (!make_tmap_576(&maps.q[l], p.q[l], static_cast<unsigned long long>(p.rows) * kHeads, kHeads))
       return DSA_ERR_CUDA;
   const long long blocks = static_cast<long long>(p.n_layers) * p.nsplit * p.rows;
-  dsa::mla::sparse_mla_tc_kernel<<<static_cast<unsigned>(blocks), dsa::mla::kThreads, dsa::mla::kSmemBytes, stream>>>(
-      maps, p);
+  if (p.kv_fp8)
+    dsa::mla::sparse_mla_tc_kernel<true>
+        <<<static_cast<unsigned>(blocks), dsa::mla::kThreads, dsa::mla::kSmemBytes, stream>>>(maps, p);
+  else
+    dsa::mla::sparse_mla_tc_kernel<false>
+        <<<static_cast<unsigned>(blocks), dsa::mla::kThreads, dsa::mla::kSmemBytes, stream>>>(maps, p);
   if (p.nsplit > 1) {
     const dim3 cgrid(kHeads, static_cast<unsigned>(static_cast<long long>(p.rows) * p.n_layers));
     dsa::attn::combine_kernel<<<cgrid, 128, 0, stream>>>(p);
@@ -381,18 +387,20 @@ dsa_status_t enqueue_attention(const dsa::attn::Params &p, int B, cudaStream_t s
 inline int B_of(int rows, int Q) { return rows / Q; }
 
 // Attention over n_layers layers (or draft steps) that share one index set.
+// kv[l] points at bf16 rows, or at FP8 latent rows when kv_fp8.
 dsa_status_t launch_attention(const DeviceState &dev, const Layout &L, uint8_t *ws, const dsa_bf16_t *const *q,
-                              const dsa_bf16_t *const *kv, dsa_bf16_t *const *out, float *const *lse, int n_layers,
+                              const void *const *kv, dsa_bf16_t *const *out, float *const *lse, int n_layers,
                               const int32_t *idx, int rows, int Q, int T, int K, float sm_scale,
-                              cudaStream_t stream, const dsa_pages_t *pages = nullptr) {
+                              cudaStream_t stream, const dsa_pages_t *pages = nullptr, bool kv_fp8 = false) {
   dsa::attn::Params p;
   std::memset(&p, 0, sizeof(p));
   for (int l = 0; l < n_layers; ++l) {
     p.q[l] = reinterpret_cast<const __nv_bfloat16 *>(q[l]);
-    p.kv[l] = reinterpret_cast<const __nv_bfloat16 *>(kv[l]);
+    p.kv[l] = kv[l];
     p.out[l] = reinterpret_cast<__nv_bfloat16 *>(out[l]);
     p.lse[l] = lse ? lse[l] : nullptr;
   }
+  p.kv_fp8 = kv_fp8 ? 1 : 0;
   p.idx = idx;
   p.n_layers = n_layers;
   p.Q = Q;
@@ -422,12 +430,13 @@ dsa_status_t launch_attention(const DeviceState &dev, const Layout &L, uint8_t *
 
 // One IndexShare group (sizes and config already checked): the indexer and
 // top-k once, then every layer over the same index set.  `pages` (nullable)
-// describes a paged key cache and paged latent caches.
+// describes a paged key cache and paged latent caches; kv[l] holds FP8
+// latent rows when kv_fp8.
 dsa_status_t group_forward(const dsa_config_t *cfg, const void *q_idx, const float *w, const void *k_idx,
-                           const int32_t *q_pos, const dsa_bf16_t *const *q, const dsa_bf16_t *const *kv,
+                           const int32_t *q_pos, const dsa_bf16_t *const *q, const void *const *kv,
                            int n_layers, int B, int Q, int T, dsa_bf16_t *const *out, int32_t *idx_out, void *ws,
                            size_t ws_bytes, cudaStream_t st, const dsa_pages_t *pages,
-                           const float *q_scale = nullptr, const float *k_scale = nullptr) {
+                           const float *q_scale = nullptr, const float *k_scale = nullptr, bool kv_fp8 = false) {
   if (n_layers < 1 || n_layers > kMaxLayers) return DSA_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * Q * n_layers > kMaxRowsY) return DSA_ERR_INVALID_ARG;
   if (!q_idx || !w || !k_idx || !q_pos || !q || !kv || !out) return DSA_ERR_INVALID_ARG;
@@ -455,7 +464,7 @@ dsa_status_t group_forward(const dsa_config_t *cfg, const void *q_idx, const flo
   DSA_TRY(launch_topk(L, wsb, scores, q_pos, B * Q, T, cfg->topk, idx, st, fuse_hist));
   // ... and every layer of the group attends over the same index set.
   return launch_attention(*dev, L, wsb, q, kv, out, nullptr, n_layers, idx, B * Q, Q, T, cfg->topk, cfg->sm_scale,
-                          st, pages);
+                          st, pages, kv_fp8);
 }
 
 }  // namespace
@@ -530,7 +539,7 @@ dsa_status_t dsa_sparse_mla_attn(const dsa_config_t *cfg, const dsa_bf16_t *q, c
       (ws == nullptr || ws_bytes < L.total))
     return DSA_ERR_WORKSPACE;
   const dsa_bf16_t *qs[1] = {q};
-  const dsa_bf16_t *kvs[1] = {kv};
+  const void *kvs[1] = {kv};
   dsa_bf16_t *outs[1] = {out};
   float *lses[1] = {lse};
   return launch_attention(*dev, L, static_cast<uint8_t *>(ws), qs, kvs, outs, lses, 1, idx, B * Q, Q, T, cfg->topk,
@@ -545,7 +554,8 @@ dsa_status_t dsa_indexshare_group_forward(const dsa_config_t *cfg, const dsa_bf1
   DSA_TRY(check_config(cfg));
   if (empty_call(B, Q, T)) return DSA_OK;
   DSA_TRY(check_sizes(B, Q, T));
-  return group_forward(cfg, q_idx, w, k_idx, q_pos, q, kv, n_layers, B, Q, T, out, idx_out, ws, ws_bytes,
+  return group_forward(cfg, q_idx, w, k_idx, q_pos, q, reinterpret_cast<const void *const *>(kv), n_layers, B, Q, T,
+                       out, idx_out, ws, ws_bytes,
                        reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
@@ -567,7 +577,7 @@ dsa_status_t dsa_mtp_draft_attn(const dsa_config_t *cfg, const int32_t *idx0, co
       (ws == nullptr || ws_bytes < L.total))
     return DSA_ERR_WORKSPACE;
   const dsa_bf16_t *qs[kMaxLayers];
-  const dsa_bf16_t *kvs[kMaxLayers];
+  const void *kvs[kMaxLayers];
   dsa_bf16_t *outs[kMaxLayers];
   const size_t qstep = static_cast<size_t>(B) * kHeads * (kLora + kRope);
   const size_t ostep = static_cast<size_t>(B) * kHeads * kLora;
@@ -615,7 +625,7 @@ dsa_status_t dsa_sparse_mla_attn_paged(const dsa_config_t *cfg, const dsa_bf16_t
       (ws == nullptr || ws_bytes < L.total))
     return DSA_ERR_WORKSPACE;
   const dsa_bf16_t *qs[1] = {q};
-  const dsa_bf16_t *kvs[1] = {kv_pool};
+  const void *kvs[1] = {kv_pool};
   dsa_bf16_t *outs[1] = {out};
   float *lses[1] = {lse};
   return launch_attention(*dev, L, static_cast<uint8_t *>(ws), qs, kvs, outs, lses, 1, idx, B * Q, Q, T, cfg->topk,
@@ -632,7 +642,8 @@ dsa_status_t dsa_indexshare_group_forward_paged(const dsa_config_t *cfg, const d
   if (empty_call(B, Q, T)) return DSA_OK;
   DSA_TRY(check_sizes(B, Q, T));
   DSA_TRY(check_pages(pages, B, T));
-  return group_forward(cfg, q_idx, w, k_pool, q_pos, q, kv_pools, n_layers, B, Q, T, out, idx_out, ws, ws_bytes,
+  return group_forward(cfg, q_idx, w, k_pool, q_pos, q, reinterpret_cast<const void *const *>(kv_pools), n_layers, B,
+                       Q, T, out, idx_out, ws, ws_bytes,
                        reinterpret_cast<cudaStream_t>(stream), pages);
 }
 
@@ -663,8 +674,49 @@ dsa_status_t dsa_indexshare_group_forward_fp8(const dsa_config_t *cfg, const uin
   DSA_TRY(check_sizes(B, Q, T));
   if (!q_scale || !k_scale) return DSA_ERR_INVALID_ARG;
   if (!aligned16(q_scale) || !aligned16(k_scale)) return DSA_ERR_ALIGNMENT;
-  return group_forward(cfg, q_idx8, w, k_idx8, q_pos, q, kv, n_layers, B, Q, T, out, idx_out, ws, ws_bytes,
+  return group_forward(cfg, q_idx8, w, k_idx8, q_pos, q, reinterpret_cast<const void *const *>(kv), n_layers, B, Q,
+                       T, out, idx_out, ws, ws_bytes,
                        reinterpret_cast<cudaStream_t>(stream), nullptr, q_scale, k_scale);
+}
+
+dsa_status_t dsa_sparse_mla_attn_fp8(const dsa_config_t *cfg, const dsa_bf16_t *q, const uint8_t *kv8,
+                                     const int32_t *idx, int B, int Q, int T, dsa_bf16_t *out, float *lse, void *ws,
+                                     size_t ws_bytes, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
+  DSA_TRY(check_sizes(B, Q, T));
+  if (!q || !kv8 || !idx || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv8) || !aligned16(idx) || !aligned16(out) || (lse && !aligned16(lse)) ||
+      (ws && !aligned16(ws)))
+    return DSA_ERR_ALIGNMENT;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  const Layout L = layout(B, Q, T, 1, cfg->topk, dev->sms);
+  if (attn_shape(static_cast<long long>(B) * Q, cfg->topk, dev->sms).nsplit > 1 &&
+      (ws == nullptr || ws_bytes < L.total))
+    return DSA_ERR_WORKSPACE;
+  const dsa_bf16_t *qs[1] = {q};
+  const void *kvs[1] = {kv8};
+  dsa_bf16_t *outs[1] = {out};
+  float *lses[1] = {lse};
+  return launch_attention(*dev, L, static_cast<uint8_t *>(ws), qs, kvs, outs, lses, 1, idx, B * Q, Q, T, cfg->topk,
+                          cfg->sm_scale, reinterpret_cast<cudaStream_t>(stream), nullptr, true);
+}
+
+dsa_status_t dsa_indexshare_group_forward_fp8kv(const dsa_config_t *cfg, const uint8_t *q_idx8,
+                                                const float *q_scale, const float *w, const uint8_t *k_idx8,
+                                                const float *k_scale, const int32_t *q_pos, const dsa_bf16_t *const *q,
+                                                const uint8_t *const *kv8, int n_layers, int B, int Q, int T,
+                                                dsa_bf16_t *const *out, int32_t *idx_out, void *ws, size_t ws_bytes,
+                                                dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
+  DSA_TRY(check_sizes(B, Q, T));
+  if (!q_scale || !k_scale) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_scale) || !aligned16(k_scale)) return DSA_ERR_ALIGNMENT;
+  return group_forward(cfg, q_idx8, w, k_idx8, q_pos, q, reinterpret_cast<const void *const *>(kv8), n_layers, B, Q,
+                       T, out, idx_out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr, q_scale,
+                       k_scale, true);
 }
 }  // extern "C"
 

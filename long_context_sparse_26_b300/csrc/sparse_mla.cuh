@@ -21,10 +21,16 @@ constexpr int kH = 64;
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kMaxLayers = 8;
+// FP8 latent row: the 512 compressed-KV dims as E4M3 codes, one fp32 scale
+// per 128-dim group, then the 64 RoPE dims kept in bf16
+constexpr int kF8Codes = 512;
+constexpr int kF8ScaleOff = 512;                  // 4 x fp32
+constexpr int kF8RopeOff = 528;                   // 64 x bf16
+constexpr int kF8RowBytes = 656;
 
 struct Params {
   const __nv_bfloat16 *q[kMaxLayers];   // [B*Q, 64, 576] per layer
-  const __nv_bfloat16 *kv[kMaxLayers];  // [B, T, 576] per layer
+  const void *kv[kMaxLayers];           // [B, T, 576] bf16 per layer, or [B, T, 656] bytes (FP8 rows)
   __nv_bfloat16 *out[kMaxLayers];       // [B*Q, 64, 512] per layer
   float *lse[kMaxLayers];               // [B*Q, 64] per layer, or null
   const int32_t *idx;                   // [B*Q, K], shared by every layer
@@ -39,6 +45,7 @@ struct Params {
   // + s % page_size of kv[l] viewed as a [num_pages * page_size, 576] pool
   const int32_t *block_table;           // [B, max_pages], shared by every layer
   int page_size, max_pages, num_pages;
+  int kv_fp8;                           // 1: kv[l] holds FP8 latent rows of kF8RowBytes
 };
 
 // Merges the splits of one (layer, row, head): O = sum_s 2^(m_s - M) O_s /

@@ -180,6 +180,7 @@ struct Small {
   uint64_t p_free;
   uint64_t q_full;
   uint64_t mma_done;
+  uint64_t staged[kProducerWarps][kStages];  // FP8 latent rows: a warp's copies of a stage have landed
   uint32_t tmem_slot;
   int abort;
   int status[2][4];               // per softmax warp, per iteration parity: 1 = ok
@@ -187,6 +188,22 @@ struct Small {
 };
 static_assert(sizeof(Small) <= kSmallBytes, "small shared region");
 
+// 16 E4M3 codes times their scale, rounded to bf16, packed in dim order.
+__device__ __forceinline__ void dequant16(const uint4 &code, float scale, uint32_t (&out)[8]) {
+  const uint32_t w[4] = {code.x, code.y, code.z, code.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu);
+      const __half2 v = __half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3));  // low byte -> .x
+      const float2 f = __half22float2(v);
+      out[2 * i + h] = pack_bf16x2(f.x * scale, f.y * scale);
+    }
+  }
+}
+
+template <bool F8KV>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -219,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm->full[i], 32 * kProducerWarps);
       mbar_init(&sm->empty[i], 1);
+      for (int w = 0; w < kProducerWarps; ++w) mbar_init(&sm->staged[w][i], 32);
     }
     // (a window j uses stages 2*(j%2) and 2*(j%2)+1)
     for (int i = 0; i < 2; ++i) {
@@ -251,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       q_issued = true;
     }
     const bool paged = p.block_table != nullptr;
-    const uint8_t *kvb = reinterpret_cast<const uint8_t *>(p.kv[layer]) + (paged ? 0 : (size_t)b * p.T * (kDv + 64) * 2);
+    constexpr size_t kRowBytes = F8KV ? attn::kF8RowBytes : (kDv + 64) * 2;
+    const uint8_t *kvb = reinterpret_cast<const uint8_t *>(p.kv[layer]) + (paged ? 0 : (size_t)b * p.T * kRowBytes);
     // row of kvb holding position pos (-1: none); the block-table load is
     // issued a stage before the row is used
     auto row_of = [&](int pos) -> int {
@@ -268,32 +287,160 @@ __global__ void __launch_bounds__(kThreads, 1)
     // in ring stage g % 4; lane l holds slot l of stage g, loaded three stages ahead
     const int nstage = nblk * kWinStages;
     auto load_slot = [&](int g) -> int { return g < nstage ? slot_raw(irow, slot0 + g * kStageRows + lane, p.K) : -1; };
-    int n1 = load_slot(0), n2 = load_slot(1), n3 = load_slot(2);
-    int next_row = row_of(checked_pos(n1, p.T, warp == 0));
-    for (int g = 0; g < nstage; ++g) {
-      const int cur = next_row;
-      n1 = n2;
-      n2 = n3;
-      n3 = load_slot(g + 3);
-      next_row = row_of(checked_pos(n1, p.T, warp == 0));
-      const int s = g % kStages;
-      const uint32_t ph = static_cast<uint32_t>(g / kStages) & 1u;
-      if (!warp_wait(&sm->empty[s], ph ^ 1u, abort_flag)) break;
-      const uint32_t sbase = smem_u32(sK) + s * kStageRows * 128;
-      for (int r = warp; r < kStageRows; r += kProducerWarps) {
-        const int pos = __shfl_sync(0xffffffffu, cur, r);
-        const uint8_t *src = kvb + (size_t)(pos < 0 ? 0 : pos) * ((kDv + 64) * 2);
-        const uint32_t nbytes = pos < 0 ? 0u : 16u;  // unused slot: zero-filled row
-        const uint32_t rbase = sbase + r * 128;       // ring row s*32 + r; (s*32 + r) % 8 == r % 8
+    if constexpr (!F8KV) {
+      int n1 = load_slot(0), n2 = load_slot(1), n3 = load_slot(2);
+      int next_row = row_of(checked_pos(n1, p.T, warp == 0));
+      for (int g = 0; g < nstage; ++g) {
+        const int cur = next_row;
+        n1 = n2;
+        n2 = n3;
+        n3 = load_slot(g + 3);
+        next_row = row_of(checked_pos(n1, p.T, warp == 0));
+        const int s = g % kStages;
+        const uint32_t ph = static_cast<uint32_t>(g / kStages) & 1u;
+        if (!warp_wait(&sm->empty[s], ph ^ 1u, abort_flag)) break;
+        const uint32_t sbase = smem_u32(sK) + s * kStageRows * 128;
+        for (int r = warp; r < kStageRows; r += kProducerWarps) {
+          const int pos = __shfl_sync(0xffffffffu, cur, r);
+          const uint8_t *src = kvb + (size_t)(pos < 0 ? 0 : pos) * kRowBytes;
+          const uint32_t nbytes = pos < 0 ? 0u : 16u;  // unused slot: zero-filled row
+          const uint32_t rbase = sbase + r * 128;       // ring row s*32 + r; (s*32 + r) % 8 == r % 8
 #pragma unroll
-        for (int cc = 0; cc < 3; ++cc) {
-          const int c = lane + 32 * cc;  // 16-byte chunk of the 1152-byte row
-          if (c < 72) cp_async_16(rbase + (c >> 3) * kPanelBytes + (((c & 7) ^ (r & 7)) << 4), src + c * 16, nbytes);
+          for (int cc = 0; cc < 3; ++cc) {
+            const int c = lane + 32 * cc;  // 16-byte chunk of the 1152-byte row
+            if (c < 72) cp_async_16(rbase + (c >> 3) * kPanelBytes + (((c & 7) ^ (r & 7)) << 4), src + c * 16, nbytes);
+          }
+        }
+        cp_async_mbar_arrive(&sm->full[s]);
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    } else {
+      // FP8 latent rows, dequantised in shared memory.  A warp owns rows
+      // warp, warp + 7, ... of every stage.  Each 656-byte row first lands by
+      // cp.async in its own ring lines (41 16-byte chunks: chunk c in panel
+      // c / 8, slot c % 8, unswizzled), tracked by the warp's own mbarrier
+      // per stage; then the warp reads its rows back, syncs, and writes the
+      // bf16 row over the same lines in the swizzled operand layout.  Only
+      // the owning warp touches a row's lines, so a warp sync orders the
+      // reads before the writes.  The warp interleaves issuing copies (as
+      // ring stages free up) with converting stages whose copies landed, so
+      // several stages stay in flight.
+      constexpr int kRPW = (kStageRows + kProducerWarps - 1) / kProducerWarps;  // rows per warp and stage
+      const uint32_t k0s = smem_u32(sK);
+      // rows of stage i (per lane: slot i*32 + lane), slot loads one issue ahead
+      int raw_cur = load_slot(0), raw_next = load_slot(1);
+      auto issue = [&](int i) {
+        const int rows_i = row_of(checked_pos(raw_cur, p.T, warp == 0));
+        raw_cur = raw_next;
+        raw_next = load_slot(i + 2);
+        const uint32_t sbase = k0s + (i % kStages) * kStageRows * 128;
+#pragma unroll
+        for (int j = 0; j < kRPW; ++j) {
+          const int r = warp + kProducerWarps * j;
+          if (r < kStageRows) {
+            const int pos = __shfl_sync(0xffffffffu, rows_i, r);
+            const uint8_t *src = kvb + (size_t)(pos < 0 ? 0 : pos) * kRowBytes;
+            const uint32_t nbytes = pos < 0 ? 0u : 16u;  // unused slot: a zero row
+            const uint32_t rbase = sbase + r * 128;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int c = lane + 32 * cc;  // chunk of the 656-byte row
+              if (c < attn::kF8RowBytes / 16) cp_async_16(rbase + (c >> 3) * kPanelBytes + (c & 7) * 16, src + c * 16, nbytes);
+            }
+          }
+        }
+        cp_async_mbar_arrive(&sm->staged[warp][i % kStages]);
+      };
+      auto convert = [&](int i) {
+        const uint32_t sbase = k0s + (i % kStages) * kStageRows * 128;
+        uint4 code[kRPW], rope[kRPW];
+        float scale[kRPW];
+#pragma unroll
+        for (int j = 0; j < kRPW; ++j) {
+          const int r = warp + kProducerWarps * j;
+          if (r < kStageRows) {
+            const uint32_t rbase = sbase + r * 128;
+            // code chunk lane; scale chunk 32 (panel 4, slot 0); RoPE chunks 33..40
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(code[j].x), "=r"(code[j].y), "=r"(code[j].z), "=r"(code[j].w)
+                         : "r"(rbase + (lane >> 3) * kPanelBytes + (lane & 7) * 16));
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(scale[j]) : "r"(rbase + 4 * kPanelBytes + 4 * (lane >> 3)));
+            const int rc = 33 + (lane & 7);
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(rope[j].x), "=r"(rope[j].y), "=r"(rope[j].z), "=r"(rope[j].w)
+                         : "r"(rbase + (rc >> 3) * kPanelBytes + (rc & 7) * 16));
+          }
+        }
+        __syncwarp();  // every lane has read its rows' staged bytes
+#pragma unroll
+        for (int j = 0; j < kRPW; ++j) {
+          const int r = warp + kProducerWarps * j;
+          if (r < kStageRows) {
+            const uint32_t rbase = sbase + r * 128;  // ring row s*32 + r; (s*32 + r) % 8 == r % 8
+            uint32_t v[8];
+            dequant16(code[j], scale[j], v);
+            // dims 16*lane..+15: panel lane/4, 16-byte chunks 2*(lane%4) and +1
+            const uint32_t pb = rbase + (lane >> 2) * kPanelBytes;
+            const int c0 = 2 * (lane & 3);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + (((c0 ^ r) & 7) << 4)), "r"(v[0]),
+                         "r"(v[1]), "r"(v[2]), "r"(v[3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + ((((c0 + 1) ^ r) & 7) << 4)),
+                         "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                         : "memory");
+            if (lane < 8)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rbase + 8 * kPanelBytes +
+                                                                             (((lane ^ r) & 7) << 4)),
+                           "r"(rope[j].x), "r"(rope[j].y), "r"(rope[j].z), "r"(rope[j].w)
+                           : "memory");
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&sm->full[i % kStages]);
+      };
+      int issued = 0, conv = 0;
+      unsigned long long t_idle = 0;
+      while (conv < nstage) {
+        bool prog = false;
+        if (issued < nstage) {
+          const uint32_t ph = static_cast<uint32_t>(issued / kStages) & 1u;
+          int ok = lane == 0 ? (mbar_try_wait(&sm->empty[issued % kStages], ph ^ 1u) ? 1 : 0) : 0;
+          if (__shfl_sync(0xffffffffu, ok, 0)) {
+            issue(issued);
+            ++issued;
+            prog = true;
+          }
+        }
+        if (conv < issued) {
+          const uint32_t ph = static_cast<uint32_t>(conv / kStages) & 1u;
+          int ok = lane == 0 ? (mbar_try_wait(&sm->staged[warp][conv % kStages], ph) ? 1 : 0) : 0;
+          if (__shfl_sync(0xffffffffu, ok, 0)) {
+            convert(conv);
+            ++conv;
+            prog = true;
+          }
+        }
+        if (prog) {
+          t_idle = 0;
+        } else {
+          int stop = 0;
+          if (lane == 0) {
+            const unsigned long long now = global_timer_ns();
+            if (t_idle == 0) {
+              t_idle = now;
+            } else if (*abort_flag) {
+              stop = 1;
+            } else if (now - t_idle > kWaitLimitNs) {
+              raise_error(kErrTimeout);
+              *abort_flag = 1;
+              stop = 1;
+            }
+          }
+          if (__shfl_sync(0xffffffffu, stop, 0)) break;
         }
       }
-      cp_async_mbar_arrive(&sm->full[s]);
+      asm volatile("cp.async.wait_all;" ::: "memory");
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
     if (q_issued && lane == 0) mbar_wait_drain(&sm->q_full, 0, kWaitLimitNs);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer

@@ -252,3 +252,27 @@ def to_e4m3_rows(x: torch.Tensor):
     scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
     codes = (xf / scale.unsqueeze(-1)).to(torch.float8_e4m3fn).view(torch.uint8)
     return codes.contiguous(), scale.contiguous()
+
+
+FP8_LATENT_ROW_BYTES = 656
+
+
+def to_fp8_latent(kv: torch.Tensor) -> torch.Tensor:
+    """Stores latent rows kv [B, T, 576] bf16 as FP8 latent rows [B, T, 656]
+    uint8: dims 0..511 as E4M3 codes with one fp32 scale per 128-dim group
+    (group amax / 448, 1 for an all-zero group) in bytes 512..527, and the 64
+    RoPE dims unchanged as bf16 in bytes 528..655.  A storage format for the
+    inputs (one sequence at a time, to bound the temporaries)."""
+    B, T, D = kv.shape
+    if D != 576 or kv.dtype != torch.bfloat16:
+        raise ValueError("latent rows are [B, T, 576] bf16")
+    out = torch.empty(B, T, FP8_LATENT_ROW_BYTES, dtype=torch.uint8, device=kv.device)
+    for b in range(B):
+        x = kv[b, :, :512].float().reshape(T, 4, 128)
+        amax = x.abs().amax(dim=-1)
+        scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+        out[b, :, :512] = (x / scale.unsqueeze(-1)).to(torch.float8_e4m3fn).view(torch.uint8).reshape(T, 512)
+        out[b, :, 512:528] = scale.contiguous().view(torch.uint8).reshape(T, 16)
+        out[b, :, 528:] = kv[b, :, 512:].contiguous().view(torch.uint8).reshape(T, 128)
+        del x, amax, scale
+    return out

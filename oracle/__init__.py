@@ -14,4 +14,6 @@ from .dsa_oracle import (  # noqa: F401
     indexer_flops,
     gather_pages,
     e4m3_to_f64,
+    fp8_latent_to_f64,
+    FP8_LATENT_ROW_BYTES,
 )

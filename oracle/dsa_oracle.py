@@ -51,6 +51,13 @@ The oracle is the plain definition of each step, written out in fp64:
   subnormals at exponent 0, S.1111.111 is NaN and nothing is infinite.  An
   FP8 cache row stands for its decoded values times its fp32 scale; the
   oracle's indexer scores are those of the decoded, scaled rows.
+* ``fp8_latent_to_f64``: the value of an FP8 latent cache row (the same
+  FP8 KV cache, here for the MLA latent rows).  The pages fix no row layout;
+  the reading taken is the one serving stacks use for MLA caches: 512
+  compressed-KV dims as E4M3 codes with one fp32 scale per 128-dim group,
+  followed by the 64 RoPE dims in bf16, 656 bytes per row.  Dim d < 512 is
+  code[d] * scale[d // 128]; the RoPE dims are their bf16 values.  The
+  oracle's attention over an FP8 cache is its attention over these values.
 * ``indexer_flops``: the indexer's multiply-add count per query token, shared
   or per layer ("GLM-5.2 技术报告解读", training-strategy table: IndexShare
   removes the indexer dot products and top-k of 3 of every 4 layers).
@@ -295,3 +302,22 @@ def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
     sub = sign * np.ldexp(m / 8.0, -6)
     v = np.where(e == 0, sub, normal)
     return np.where((e == 15) & ((c & 0x7) == 7), np.nan, v)
+
+
+FP8_LATENT_ROW_BYTES = 656
+
+
+def fp8_latent_to_f64(rows: np.ndarray) -> np.ndarray:
+    """Values [..., 576] (fp64) of FP8 latent rows [..., 656] (uint8): bytes
+    0..511 are E4M3 codes of dims 0..511, bytes 512..527 four little-endian
+    fp32 scales (dims 128g..128g+127 use scale g), bytes 528..655 the 64 RoPE
+    dims as little-endian bf16."""
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.uint8))
+    if r.shape[-1] != FP8_LATENT_ROW_BYTES:
+        raise ValueError("FP8 latent rows are 656 bytes")
+    lead = r.shape[:-1]
+    codes = e4m3_to_f64(r[..., :512]).reshape(*lead, 4, 128)
+    scales = np.ascontiguousarray(r[..., 512:528]).view("<f4").astype(np.float64)  # [..., 4]
+    nope = (codes * scales[..., None]).reshape(*lead, 512)
+    rope = bf16_bits_to_f64(np.ascontiguousarray(r[..., 528:656]).view("<u2"))       # [..., 64]
+    return np.concatenate([nope, rope], axis=-1)

@@ -54,7 +54,7 @@ def test_fp8_indexer_scores(B, Q, T, first):
             check_scores_row(g[b, t], ora[b, t], int(pos[b, t]))
 
 
-def _fp8_group_check(w_, rows=None):
+def _fp8_group_check(w_, rows=None, fp8_kv=False):
     cfg = dsa.default_config(topk=w_.topk)
     inp = wl.make_inputs(w_, DEV)
     B, Q, T = w_.B, w_.Q, w_.T
@@ -63,7 +63,15 @@ def _fp8_group_check(w_, rows=None):
     outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV) for _ in range(w_.n_layers)]
     idx = torch.empty(B, Q, w_.topk, dtype=torch.int32, device=DEV)
     ws = dsa.alloc_workspace(cfg, B, Q, T, w_.n_layers)
-    dsa.indexshare_group_forward_fp8(cfg, q8, q_scale, inp.w, k8, k_scale, inp.q_pos, inp.q, inp.kv, outs, idx, ws)
+    if fp8_kv:
+        kv8s = [wl.to_fp8_latent(kv) for kv in inp.kv]
+        inp.kv = None
+        torch.cuda.empty_cache()
+        dsa.indexshare_group_forward_fp8kv(cfg, q8, q_scale, inp.w, k8, k_scale, inp.q_pos, inp.q, kv8s, outs, idx,
+                                           ws)
+    else:
+        dsa.indexshare_group_forward_fp8(cfg, q8, q_scale, inp.w, k8, k_scale, inp.q_pos, inp.q, inp.kv, outs, idx,
+                                         ws)
     torch.cuda.synchronize()
     g_idx = idx.cpu().numpy()
     rows = rows if rows is not None else [(b, t) for b in range(B) for t in range(Q)]
@@ -76,7 +84,11 @@ def _fp8_group_check(w_, rows=None):
         ties += check_topk_row(g_idx[b, t], o_idx, S, pos, w_.topk)
         gv = g_idx[b, t][g_idx[b, t] >= 0]
         for layer in range(w_.n_layers):
-            rows_kv = f64(inp.kv[layer][b, torch.from_numpy(gv).to(DEV)])
+            sel = torch.from_numpy(gv).to(DEV)
+            if fp8_kv:
+                rows_kv = oracle.fp8_latent_to_f64(kv8s[layer][b, sel].cpu().numpy())
+            else:
+                rows_kv = f64(inp.kv[layer][b, sel])
             O, _ = oracle.sparse_mla_attn_row(f64(inp.q[layer][b, t]), rows_kv, np.arange(gv.size), wl.SM_SCALE)
             check_attention(f64(outs[layer][b, t]), O)
     return ties
@@ -91,7 +103,77 @@ def test_fp8_group_tiny():
     _fp8_group_check(wl.TINY)
 
 
+def test_fp8kv_group_decode():
+    import dataclasses
+    _fp8_group_check(dataclasses.replace(wl.DECODE_128K, name="fp8kv_small", B=3, T=50_000, first_pos=49_999),
+                     fp8_kv=True)
+
+
+def test_fp8kv_group_verify_small():
+    import dataclasses
+    _fp8_group_check(dataclasses.replace(wl.VERIFY, name="fp8kv_verify", B=2, T=20_000, first_pos=19_992),
+                     fp8_kv=True)
+
+
+# FP8 latent rows: one layer against the oracle on the values the rows stand for
+@pytest.mark.parametrize("B,Q,T,k,pad", [
+    (1, 1, 5000, 2048, 0),       # one row: many splits
+    (2, 2, 9000, 2048, 37),      # padding slots
+    (3, 1, 3000, 100, 0),        # ragged last block
+    (1, 1, 40, 2048, 0),         # fewer rows than slots
+    (40, 8, 2500, 256, 0),       # many rows: single split, no combine
+])
+def test_fp8_latent_attention(B, Q, T, k, pad):
+    cfg = dsa.default_config(topk=k)
+    seed = B * 1000 + T + 7
+    q = wl.mla_queries(B, Q, seed, 0, DEV)
+    kv8 = wl.to_fp8_latent(wl.latent_cache(B, T, seed, 0, DEV))
+    rng = np.random.default_rng(seed)
+    idx = np.full((B, Q, k), -1, dtype=np.int32)
+    for b in range(B):
+        for t in range(Q):
+            n = k - pad if k - pad <= T else T
+            idx[b, t, :n] = np.sort(rng.choice(T, n, replace=False))
+    out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, Q, 64, dtype=torch.float32, device=DEV)
+    dsa.sparse_mla_attn_fp8(cfg, q, kv8, torch.from_numpy(idx).to(DEV), out, lse,
+                            dsa.alloc_workspace(cfg, B, Q, T, 1))
+    torch.cuda.synchronize()
+    O, LSE = oracle.sparse_mla_attn(f64(q), oracle.fp8_latent_to_f64(kv8.cpu().numpy()), idx, wl.SM_SCALE)
+    check_attention(f64(out), O)
+    assert np.abs(lse.cpu().double().numpy() - LSE).max() < 1e-3
+
+
+def test_fp8_latent_zero_group_and_empty_row():
+    """A row with an all-zero group (scale 1, codes 0; every other group's amax
+    is the largest code, 448 x scale), and a query row with no valid slot."""
+    cfg = dsa.default_config(topk=64)
+    B, Q, T = 1, 2, 300
+    kv = wl.latent_cache(B, T, 5, 0, DEV)
+    kv[0, 10, :128] = 0
+    kv8 = wl.to_fp8_latent(kv)
+    assert int(kv8[0, 10, :128].max()) == 0 and (kv8[0, 11, :128] & 0x7F).max() == 0x7E
+    q = wl.mla_queries(B, Q, 5, 0, DEV)
+    idx = torch.full((B, Q, 64), -1, dtype=torch.int32, device=DEV)
+    idx[0, 0, :6] = torch.tensor([0, 10, 11, 150, 298, 299], dtype=torch.int32)
+    out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, Q, 64, device=DEV)
+    dsa.sparse_mla_attn_fp8(cfg, q, kv8, idx, out, lse, dsa.alloc_workspace(cfg, B, Q, T, 1))
+    torch.cuda.synchronize()
+    O, _ = oracle.sparse_mla_attn(f64(q), oracle.fp8_latent_to_f64(kv8.cpu().numpy()), idx.cpu().numpy(),
+                                  wl.SM_SCALE)
+    check_attention(f64(out[:, :1]), O[:, :1])
+    assert torch.all(out[0, 1] == 0)
+    assert torch.all(torch.isneginf(lse[0, 1]))
+
+
 def test_full_decode_1m_fp8_sampled():
     ties = _fp8_group_check(wl.DECODE_1M, rows=[(0, 0), (5, 0)])
     print("boundary ties at 1M (fp8):", ties)
+    torch.cuda.empty_cache()
+
+
+def test_full_decode_1m_fp8kv_sampled():
+    ties = _fp8_group_check(wl.DECODE_1M, rows=[(2, 0), (7, 0)], fp8_kv=True)
+    print("boundary ties at 1M (fp8 caches):", ties)
     torch.cuda.empty_cache()

@@ -331,12 +331,34 @@ def pin_e4m3_decoding(o):
     assert np.all(np.diff(pos) > 0)
 
 
+def pin_fp8_latent_rows(o):
+    """A 656-byte FP8 latent row written byte by byte: codes, four group scales, bf16 RoPE dims."""
+    import struct
+    row = bytearray(656)
+    codes = {0: 0x38, 127: 0x40, 128: 0x3C, 300: 0xB8, 511: 0x7E, 200: 0x01}   # 1, 2, 1.5, -1, 448, 2^-9
+    for d, c in codes.items():
+        row[d] = c
+    row[512:528] = struct.pack("<4f", 0.5, 2.0, 0.25, 4.0)
+    for j, bits in {0: 0x3F80, 10: 0x4049, 63: 0xC000}.items():             # 1.0, 3.140625, -2.0
+        row[528 + 2 * j: 530 + 2 * j] = struct.pack("<H", bits)
+    want = np.zeros(576)
+    want[0], want[127], want[128], want[300], want[511], want[200] = 0.5, 1.0, 3.0, -0.25, 1792.0, 2.0 ** -9 * 2.0
+    want[512], want[522], want[575] = 1.0, 3.140625, -2.0
+    arr = np.frombuffer(bytes(row), dtype=np.uint8)
+    got = o.fp8_latent_to_f64(arr)
+    assert got.shape == (576,) and np.array_equal(got, want), np.nonzero(got != want)
+    # leading dims are kept, rows decode independently
+    two = np.stack([arr, np.zeros(656, np.uint8)]).reshape(2, 1, 656)
+    g2 = o.fp8_latent_to_f64(two)
+    assert g2.shape == (2, 1, 576) and np.array_equal(g2[0, 0], want) and not g2[1].any()
+
+
 PINS = [
     pin_bf16_conversion, pin_indexer_golden, pin_indexer_closed_form, pin_indexer_bruteforce,
     pin_topk_golden, pin_topk_bruteforce, pin_topk_k_covers_row, pin_attn_golden,
     pin_attn_dense_special_case, pin_attn_one_hot_and_identical, pin_attn_permutation,
     pin_group_reuses_one_index_set, pin_per_layer_variant, pin_mtp_reuse_and_kv_share,
-    pin_indexer_flops, pin_gather_pages, pin_e4m3_decoding,
+    pin_indexer_flops, pin_gather_pages, pin_e4m3_decoding, pin_fp8_latent_rows,
 ]
 
 
@@ -446,6 +468,16 @@ def _mut_pages_row_major(pool, block_table, T):
     return out
 
 
+def _mut_fp8_groups_of_64(rows):
+    r = np.asarray(rows, dtype=np.uint8)
+    lead = r.shape[:-1]
+    scales = np.ascontiguousarray(r[..., 512:528]).view("<f4").astype(np.float64)
+    per_dim = scales[..., (np.arange(512) // 64) % 4]
+    nope = dsa_oracle.e4m3_to_f64(r[..., :512]) * per_dim
+    rope = dsa_oracle.bf16_bits_to_f64(np.ascontiguousarray(r[..., 528:656]).view("<u2"))
+    return np.concatenate([nope.reshape(*lead, 512), rope], axis=-1)
+
+
 MUTANTS = {
     "relu_after_head_sum": ("indexer_scores_row", _mut_relu_after_sum),
     "causal_mask_excludes_self": ("indexer_scores_row", _mut_mask_excludes_self),
@@ -461,6 +493,7 @@ MUTANTS = {
     "indexer_never_shared": ("indexer_flops", _mut_flops_per_layer_always),
     "pages_interleaved": ("gather_pages", _mut_pages_row_major),
     "e4m3_bias_8": ("e4m3_to_f64", lambda codes, _f=dsa_oracle.e4m3_to_f64: _f(codes) / 2.0),
+    "fp8_latent_groups_of_64": ("fp8_latent_to_f64", _mut_fp8_groups_of_64),
 }
 
 
