@@ -354,7 +354,6 @@ dsa_status_t launch_topk(const Layout &L, uint8_t *ws, const float *scores, cons
     if (clear_topk_state(L, ws, stream) != DSA_OK) return DSA_ERR_CUDA;
     topk_chunk_hist_kernel<<<grid, kThreads, 0, stream>>>(p);
   }
-  topk_plan_kernel<<<rows, kThreads, 0, stream>>>(p);
   topk_chunk_scan_kernel<1><<<grid, kThreads, 0, stream>>>(p);
   topk_chunk_scan_kernel<2><<<grid, kThreads, 0, stream>>>(p);
   topk_chunk_select_kernel<<<rows, kThreads, kSelectSmem, stream>>>(p);

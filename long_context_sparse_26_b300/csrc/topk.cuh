@@ -30,11 +30,11 @@
 // Two launch shapes:
 //   * many rows (prefill): one block per row does every step in shared memory;
 //   * few long rows (decode): (chunk, row) blocks count step 1 (or it comes
-//     fused from the indexer), one block per row reads the histogram once and
-//     writes the row's plan (b0, need, whether bin b0 is taken whole), then
-//     (chunk, row) blocks do steps 2-3, each writing its candidates in order
-//     into its own chunk's slice of a per-row buffer plus a count, and one
-//     block per row gathers the chunks in order and does step 4.  Passes are
+//     fused from the indexer); then (chunk, row) blocks each derive the row's
+//     plan (b0, need, whether bin b0 is taken whole) from the complete
+//     histogram and do steps 2-3, each writing its candidates in order into
+//     its own chunk's slice of a per-row buffer plus a count, and one block
+//     per row gathers the chunks in order and does step 4.  Passes are
 //     separate launches in stream order; no block waits on another.
 // If a row still has more candidates than the select buffer holds (thousands
 // of exactly equal scores), three exact radix passes over the row and an
@@ -198,6 +198,58 @@ __device__ __forceinline__ RowPlan plan_row(const uint32_t *hist0, uint32_t K, S
   return r;
 }
 
+// plan_row over a digit-0 histogram in global memory, with coalesced reads:
+// warp w owns bins [512w, 512w + 512), lane l reads bins 512w + 32j + l.  The
+// warp holding the k-th largest key then walks its bins from the top, 32 at a
+// time, with a lane suffix sum.
+__device__ __forceinline__ RowPlan plan_row_global(const uint32_t *g, uint32_t K, Scratch *sc) {
+  static_assert(kBins0 == (kThreads / 32) * 512, "one 512-bin slice per warp");
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  uint32_t h[16];
+  uint32_t tot = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    h[j] = __ldg(g + w * 512 + 32 * j + l);
+    tot += h[j];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+  if (l == 0) sc->warp_a[w] = tot;
+  __syncthreads();
+  uint32_t above = 0;
+  for (int v = w + 1; v < kThreads / 32; ++v) above += sc->warp_a[v];
+  if (above < K && K <= above + sc->warp_a[w]) {
+    uint32_t cum = above;  // count in the bins above the current round
+#pragma unroll
+    for (int j = 15; j >= 0; --j) {
+      uint32_t suf = h[j];  // this lane's bin plus the higher lanes' bins of the round
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t n = __shfl_down_sync(0xffffffffu, suf, off);
+        if (l + off < 32) suf += n;
+      }
+      const uint32_t round_total = __shfl_sync(0xffffffffu, suf, 0);
+      if (cum + round_total >= K) {
+        if (cum + suf - h[j] < K && K <= cum + suf) {
+          sc->result[0] = static_cast<uint32_t>(w * 512 + 32 * j + l);
+          sc->result[1] = K - (cum + suf - h[j]);
+          sc->result[2] = h[j];
+        }
+        break;
+      }
+      cum += round_total;
+    }
+  }
+  __syncthreads();
+  RowPlan r;
+  r.b0 = sc->result[0];
+  r.need1 = sc->result[1];
+  const uint32_t bin = sc->result[2];
+  r.take_b0 = r.need1 == bin || (K - r.need1) + bin <= static_cast<uint32_t>(kSmemCand);
+  __syncthreads();
+  return r;
+}
+
 // One pass over [start, end) that appends the composites of the chosen
 // elements to dst[0 ..] in position order; entries at or past `cap` are
 // counted but not written.  PASS 1 chooses digit 0 > b0 (>= b0 with
@@ -221,7 +273,6 @@ __device__ uint32_t scan_ordered(const float *srow, int start, int end, const Ro
 #pragma unroll
       for (int u = 0; u < 8; ++u) val[u] = i0 + u < end ? __ldg(srow + i0 + u) : 0.0f;
     }
-    uint64_t comp[8];
     uint32_t takes = 0;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -237,14 +288,13 @@ __device__ uint32_t scan_ordered(const float *srow, int start, int end, const Ro
         t = in && d0 == rp.b0 && d1 >= b1;
       }
       takes |= (t ? 1u : 0u) << u;
-      comp[u] = composite(key, static_cast<uint32_t>(i));
     }
     uint32_t tot;
     uint32_t off = count + block_exclusive_sum(__popc(takes), &tot, sc);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if ((takes >> u) & 1u) {
-        if (off < cap) dst[off] = comp[u];
+        if (off < cap) dst[off] = composite(score_key(val[u]), static_cast<uint32_t>(i0 + u));
         ++off;
       }
     }
@@ -256,10 +306,13 @@ __device__ uint32_t scan_ordered(const float *srow, int start, int end, const Ro
 // Exact k-th largest composite among src[0..n) (1 <= k <= n): radix passes of
 // 11-bit digits from the top, stopping as soon as the threshold bin is taken
 // whole.  Every composite >= the returned value is selected: exactly k.
-__device__ uint64_t select_threshold(const uint64_t *src, uint32_t n, uint32_t k, uint32_t *hist, Scratch *sc) {
-  uint64_t prefix = 0, known = 0;
+// The search may start with the top bits already known: composites matching
+// `prefix` on `known` are the ones still in play and the k-th largest of them
+// is sought, from digit position first_shift down.
+__device__ uint64_t select_threshold(const uint64_t *src, uint32_t n, uint32_t k, uint32_t *hist, Scratch *sc,
+                                     uint64_t prefix = 0, uint64_t known = 0, int first_shift = 53) {
   uint32_t need = k;
-  for (int shift = 53;; shift -= 11) {
+  for (int shift = first_shift;; shift -= 11) {
     const int sh = shift < 0 ? 0 : shift;
     const int width = shift < 0 ? 11 + shift : 11;
     const uint64_t dmask = (1ull << width) - 1ull;
@@ -387,9 +440,14 @@ __device__ void write_ordered(const uint64_t *src, uint32_t n, uint64_t tau, int
 }
 
 // Step 4 on n candidates in shared memory (position-ordered when `ordered`).
-__device__ void finish_row(const uint64_t *cand, uint32_t n, int K, bool ordered, const SmemViews &s, int32_t *out,
-                           Scratch *sc) {
-  const uint64_t tau = select_threshold(cand, n, static_cast<uint32_t>(K), s.hist, sc);
+// The plan already fixes digit 0 of the k-th composite (bin b0, composite
+// bits 63..51) and its rank within that bin (need1), so the search starts
+// inside bin b0 at composite bit 50.
+__device__ void finish_row(const uint64_t *cand, uint32_t n, int K, const RowPlan &rp, bool ordered,
+                           const SmemViews &s, int32_t *out, Scratch *sc) {
+  (void)K;
+  const uint64_t tau = select_threshold(cand, n, rp.need1, s.hist, sc, static_cast<uint64_t>(rp.b0) << 51,
+                                        0x1FFFull << 51, 40);
   if (ordered)
     write_ordered(cand, n, tau, out, sc);
   else
@@ -431,7 +489,7 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const float *__restr
     row_select_multipass(srow, L, K, out, s.hist, &sc);
     return;
   }
-  finish_row(s.cand, n, K, rp.take_b0, s, out, &sc);
+  finish_row(s.cand, n, K, rp, rp.take_b0, s, out, &sc);
 }
 
 // --------------------------------------------------------------------------
@@ -469,25 +527,6 @@ __global__ void __launch_bounds__(kThreads) topk_chunk_hist_kernel(const ChunkPa
     if (hist[i]) atomicAdd(g + i, hist[i]);
 }
 
-// One block per row: the row's plan from its digit-0 histogram.
-__global__ void __launch_bounds__(kThreads) topk_plan_kernel(const ChunkParams p) {
-  __shared__ uint32_t hist[kBins0];
-  __shared__ Scratch sc;
-  const int row = blockIdx.x;
-  const int L = visible_length(p.q_pos, row, p.T);
-  if (L <= p.K) return;
-  const uint32_t *g0 = p.ghist + (size_t)row * kGhistStride;
-  for (int i = threadIdx.x; i < kBins0; i += kThreads) hist[i] = g0[i];
-  __syncthreads();
-  const RowPlan rp = plan_row(hist, static_cast<uint32_t>(p.K), &sc);
-  if (threadIdx.x == 0) {
-    uint32_t *pl = p.plan + (size_t)row * 4;
-    pl[0] = rp.b0;
-    pl[1] = rp.need1;
-    pl[2] = rp.take_b0 ? 1u : 0u;
-  }
-}
-
 __device__ __forceinline__ RowPlan load_plan(const ChunkParams &p, int row) {
   const uint32_t *pl = p.plan + (size_t)row * 4;
   RowPlan rp;
@@ -510,7 +549,21 @@ __global__ void __launch_bounds__(kThreads) topk_chunk_scan_kernel(const ChunkPa
   if (L <= p.K || start >= L) return;
   const int end = min(start + p.chunk, L);
   uint32_t *g1 = p.ghist + (size_t)row * kGhistStride + kBins0;
-  const RowPlan rp = load_plan(p, row);
+  // pass 1: every block of the row derives the row's plan from its complete
+  // digit-0 histogram (the same in each block); chunk 0 records it for the
+  // later kernels
+  RowPlan rp;
+  if (PASS == 1) {
+    rp = plan_row_global(p.ghist + (size_t)row * kGhistStride, static_cast<uint32_t>(p.K), &sc);
+    if (c == 0 && threadIdx.x == 0) {
+      uint32_t *pl = p.plan + (size_t)row * 4;
+      pl[0] = rp.b0;
+      pl[1] = rp.need1;
+      pl[2] = rp.take_b0 ? 1u : 0u;
+    }
+  } else {
+    rp = load_plan(p, row);
+  }
   if (PASS == 2 && rp.take_b0) return;  // single-pass row
   uint32_t b1 = 0;
   if (PASS == 1) {
@@ -571,7 +624,7 @@ __global__ void __launch_bounds__(kThreads) topk_chunk_select_kernel(const Chunk
     for (uint32_t i = lane; i < m; i += 32) s.cand[o + i] = src[i];
   }
   __syncthreads();
-  finish_row(s.cand, n, p.K, rp.take_b0, s, out, &sc);
+  finish_row(s.cand, n, p.K, rp, rp.take_b0, s, out, &sc);
 }
 
 }  // namespace topk
