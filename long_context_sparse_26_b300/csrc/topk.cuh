@@ -261,6 +261,16 @@ __device__ uint32_t scan_ordered(const float *srow, int start, int end, const Ro
   uint32_t count = 0;
   // 16-byte loads when the row is 16-byte aligned (starts are multiples of 8)
   const bool vec = (reinterpret_cast<uintptr_t>(srow + start) & 15u) == 0 && (start & 7) == 0;
+  // Pass 1 compares floats: score_key is monotonic (with -0 folded onto +0,
+  // which compare equal as floats too), so "digit 0 >= d" is "score >= the
+  // smallest float of bin d".  NaN (no bin above the top one, and the fill
+  // past `end`) compares false.
+  const float kNever = __uint_as_float(0x7FFFFFFFu);
+  auto bin_floor = [](uint32_t d) -> float {
+    const uint32_t k = d << kShift0;
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+  };
+  const float thr = rp.take_b0 ? bin_floor(rp.b0) : (rp.b0 + 1 < static_cast<uint32_t>(kBins0) ? bin_floor(rp.b0 + 1) : kNever);
   for (int base = start; base < end; base += kThreads * 8) {  // block-uniform trip count
     const int i0 = base + threadIdx.x * 8;                   // 8 consecutive elements per thread
     float val[8];
@@ -271,23 +281,26 @@ __device__ uint32_t scan_ordered(const float *srow, int start, int end, const Ro
       val[4] = c.x; val[5] = c.y; val[6] = c.z; val[7] = c.w;
     } else {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) val[u] = i0 + u < end ? __ldg(srow + i0 + u) : 0.0f;
+      for (int u = 0; u < 8; ++u) val[u] = i0 + u < end ? __ldg(srow + i0 + u) : kNever;
     }
     uint32_t takes = 0;
+    if (PASS == 1) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u;
-      const bool in = i < end;
-      const uint32_t key = score_key(val[u]);
-      const uint32_t d0 = key >> kShift0, d1 = (key >> kShift1) & (kBins - 1);
-      bool t;
-      if (PASS == 1) {
-        t = in && (d0 > rp.b0 || (rp.take_b0 && d0 == rp.b0));
-        if (hist1 != nullptr && in && d0 == rp.b0) atomicAdd(&hist1[d1], 1u);
-      } else {
-        t = in && d0 == rp.b0 && d1 >= b1;
+      for (int u = 0; u < 8; ++u) takes |= (val[u] >= thr ? 1u : 0u) << u;
+      if (hist1 != nullptr) {  // two-pass row: digit 1 of bin b0
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t key = score_key(val[u]);
+          if (i0 + u < end && (key >> kShift0) == rp.b0) atomicAdd(&hist1[(key >> kShift1) & (kBins - 1)], 1u);
+        }
       }
-      takes |= (t ? 1u : 0u) << u;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t key = score_key(val[u]);
+        const bool t = i0 + u < end && (key >> kShift0) == rp.b0 && ((key >> kShift1) & (kBins - 1)) >= b1;
+        takes |= (t ? 1u : 0u) << u;
+      }
     }
     uint32_t tot;
     uint32_t off = count + block_exclusive_sum(__popc(takes), &tot, sc);
