@@ -470,43 +470,82 @@ def run_e2e(args, w, cfg, inp, outs, idx, scores, ws, stream, dsa) -> dict:
     """Per step: pinned host -> device copy of the step's new inputs (query-side
     tensors; the indexer key cache and latent caches stay resident in HBM as
     the model's state), the step through the C ABI, device -> host copy of the
-    outputs.  Timed with events on the stream."""
+    outputs.  As a serving loop would, the copies run on their own streams,
+    double-buffered: step i+1's inputs go up and step i-1's outputs come down
+    while step i computes.  Every step's copies lie inside the timed region
+    (events on the compute stream, which waits for the last download)."""
+    dev = stream.device
     if w.kind == "mtp":
-        dev_in = [inp.q_idx, inp.w, inp.q_pos, inp.q_steps]
+        dev_in0 = [inp.q_idx, inp.w, inp.q_pos, inp.q_steps]
     else:
-        dev_in = [inp.q_idx, inp.w, inp.q_pos] + list(inp.q)
-    host_in = [t.detach().cpu().pin_memory() for t in dev_in]
-    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        dev_in0 = [inp.q_idx, inp.w, inp.q_pos] + list(inp.q)
+    host_in = [t.detach().cpu().pin_memory() for t in dev_in0]
+    host_out = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs] for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    dev_in = [dev_in0, [torch.empty_like(t) for t in dev_in0]]
+    dev_out = [outs, [torch.empty_like(o) for o in outs]]
+    torch.cuda.synchronize()
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready, done, out_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
-    def one():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
+    def upload(k, after):
+        up.wait_event(after)
+        with torch.cuda.stream(up):
+            for d, h in zip(dev_in[k], host_in):
+                d.copy_(h, non_blocking=True)
+        in_ready[k].record(up)
+
+    def compute(k):
+        stream.wait_event(in_ready[k])
+        stream.wait_event(out_free[k])   # the previous download of this output set
+        d_in, o = dev_in[k], dev_out[k]
         if w.kind == "mtp":
-            dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, stream)
-            dsa.topk_select(cfg, scores, inp.q_pos, idx, ws, stream)
-            dsa.mtp_draft_attn(cfg, idx, inp.q_steps, inp.kv[0], outs[0], ws, stream)
+            q_idx, wt, q_pos, q_steps = d_in
+            dsa.indexer_scores(cfg, q_idx, wt, inp.k_idx, q_pos, scores, stream)
+            dsa.topk_select(cfg, scores, q_pos, idx, ws, stream)
+            dsa.mtp_draft_attn(cfg, idx, q_steps, inp.kv[0], o[0], ws, stream)
         else:
-            dsa.indexshare_group_forward(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, inp.q, inp.kv, outs, idx,
-                                         ws, stream)
-        for h, o in zip(host_out, outs):
-            h.copy_(o, non_blocking=True)
+            q_idx, wt, q_pos, qs = d_in[0], d_in[1], d_in[2], d_in[3:]
+            dsa.indexshare_group_forward(cfg, q_idx, wt, inp.k_idx, q_pos, qs, inp.kv, o, idx, ws, stream)
+        done[k].record(stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            one()
-        stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            one()
-        e1.record(stream)
+    def download(k):
+        down.wait_event(done[k])
+        with torch.cuda.stream(down):
+            for h, o in zip(host_out[k], dev_out[k]):
+                h.copy_(o, non_blocking=True)
+        out_free[k].record(down)
+
+    def run(n, start_event):
+        for k in range(2):
+            out_free[k].record(stream)
+        upload(0, start_event)
+        for i in range(n):
+            k = i & 1
+            if i + 1 < n:
+                # the other input set is free once step i-1 has computed
+                upload(1 - k, done[1 - k] if i >= 1 else start_event)
+            compute(k)
+            download(k)
+        stream.wait_event(out_free[(n - 1) & 1])
+        stream.wait_event(out_free[n & 1] if n >= 2 else out_free[(n - 1) & 1])
+
+    s0 = torch.cuda.Event()
+    s0.record(stream)
+    run(max(3, args.warmup), s0)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(args.steps, e0)
+    e1.record(stream)
     stream.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     tokens = w.B * w.Q if w.kind != "mtp" else w.B * w.mtp_steps
     return {"value": tokens / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "api": "long_context_sparse_26_b300.binding (C ABI via ctypes)"}
+            "d2h_bytes_per_step": d2h, "api": "long_context_sparse_26_b300.binding (C ABI via ctypes)",
+            "overlap": "double-buffered: uploads and downloads on their own streams, overlapping compute"}
 
 
 def run_per_layer_variant(args, w, cfg, inp, dev, group_ms, dsa) -> dict:
