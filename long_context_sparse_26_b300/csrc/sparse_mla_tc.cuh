@@ -37,8 +37,12 @@
 // on some scheduler, which caps a thread at 168 registers):
 //   producers  rows w, w + kProducerWarps, ... of each stage; warp 0 also
 //              loads the query panels by TMA;
-//   next warp  tensor-memory allocation and MMA issue (one thread);
-//   last 4     softmax, O^T rescale, epilogue; warp w owns TMEM lanes
+//   next warp  tensor-memory allocation and GEMM 1 issue (one thread);
+//   last 4     softmax, O^T rescale, epilogue; the first of them also issues
+//              GEMM 2 (one thread), so that GEMM 1 of the next window and
+//              GEMM 2 of this one are issued side by side (one thread issues
+//              these small MMAs at ~54 cycles each, two reach the ~32-48
+//              cycles their shared-memory operands take); warp w owns TMEM lanes
 //              32*(w%4)..+31: heads 16*(w%4)..+15 of S (an M = 64 result
 //              sits in lanes 0-15 of each 32-lane quarter) and dims
 //              128c + 32*(w%4)..+31 of O^T chunk c.
@@ -180,6 +184,7 @@ struct Small {
   uint64_t p_free;
   uint64_t q_full;
   uint64_t mma_done;
+  uint64_t mma2_done;
   uint64_t staged[kProducerWarps][kStages];  // FP8 latent rows: a warp's copies of a stage have landed
   uint32_t tmem_slot;
   int abort;
@@ -247,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm->p_free, 1);
     mbar_init(&sm->q_full, 1);
     mbar_init(&sm->mma_done, 1);
+    mbar_init(&sm->mma2_done, 1);
     sm->abort = 0;
     fence_mbar_init();
   }
@@ -446,70 +452,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nblk > 0) {
       constexpr uint32_t id1 = idesc(64, kKeys, false, false);
-      constexpr uint32_t id2 = idesc(128, 64, true, false);
-      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), p0 = smem_u32(sP);
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK);
       bool ok = mbar_wait_bounded(&sm->q_full, 0, abort_flag);
-      // Issue whichever is ready: GEMM 2 of window g2 once its P is written
-      // (first: it unblocks the softmax), else GEMM 1 of window g1 once its
-      // rows have landed and its S buffer is free.  A fixed order would let a
-      // window still being gathered hold up the softmax of the previous one.
-      int g1 = 0, g2 = 0;
-      unsigned long long t_idle = 0;
-      while (ok && g2 < nblk) {
-        bool progressed = false;
-        if (g2 < g1 && mbar_try_wait(&sm->p_full, static_cast<uint32_t>(g2) & 1u)) {
-          tc_fence_after();
-          const int w = g2 % kWindows;
-          const uint32_t ks = k0 + w * kKeys * 128;
+      // GEMM 1 of each window in order, once its rows have landed and its S
+      // buffer is free; GEMM 2 is issued by the first softmax warp, so the two
+      // GEMMs of neighbouring windows are issued side by side (one issuing
+      // thread cannot keep the tensor pipe fed with these small MMAs)
+      for (int g1 = 0; ok && g1 < nblk; ++g1) {
+        const int w = g1 % kWindows;  // window slot in the ring
+        const int sb = g1 & 1;        // S buffer
+        const uint32_t ph = static_cast<uint32_t>(g1 / kWindows) & 1u;
+        ok = mbar_wait_bounded(&sm->s_empty[sb], (static_cast<uint32_t>(g1 >> 1) & 1u) ^ 1u, abort_flag);
+        for (int h = 0; h < kWinStages && ok; ++h) ok = mbar_wait_bounded(&sm->full[w * kWinStages + h], ph, abort_flag);
+        if (!ok) break;
+        fence_proxy_async_smem();  // the gathered rows were written through the generic proxy
+        tc_fence_after();
+        const uint32_t d = tmem_base + kSCol + sb * kKeys;
+        const uint32_t ks = k0 + w * kKeys * 128;  // the window's rows in every panel
 #pragma unroll
-          for (int c = 0; c < kDv / 128; ++c) {
-#pragma unroll
-            for (int kk = 0; kk < kKeys / 16; ++kk) {
-              const uint64_t ad = desc_sw128(ks + 2 * c * kPanelBytes + kk * 16 * 128, kPanelBytes, 1024);
-              const uint64_t bd = desc_sw128(p0 + kk * 32, 16, 1024);
-              tc_mma_bf16(tmem_base + kOCol + c * 64, ad, bd, id2, (g2 > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
-          for (int h = 0; h < kWinStages; ++h) tc_commit(&sm->empty[w * kWinStages + h]);
-          tc_commit(&sm->p_free);
-          ++g2;
-          progressed = true;
-        } else if (g1 < nblk) {
-          const int w = g1 % kWindows;  // window slot in the ring
-          const int sb = g1 & 1;        // S buffer
-          const uint32_t ph = static_cast<uint32_t>(g1 / kWindows) & 1u;
-          bool ready = mbar_try_wait(&sm->s_empty[sb], (static_cast<uint32_t>(g1 >> 1) & 1u) ^ 1u);
-          for (int h = 0; h < kWinStages && ready; ++h) ready = mbar_try_wait(&sm->full[w * kWinStages + h], ph);
-          if (ready) {
-            fence_proxy_async_smem();  // the gathered rows were written by cp.async (generic proxy)
-            tc_fence_after();
-            const uint32_t d = tmem_base + kSCol + sb * kKeys;
-            const uint32_t ks = k0 + w * kKeys * 128;  // the window's rows in every panel
-#pragma unroll
-            for (int kk = 0; kk < kPanels * 4; ++kk) {
-              const uint32_t qoff = (kk >> 2) * (kH * 128) + (kk & 3) * 32;
-              const uint32_t koff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-              tc_mma_bf16(d, desc_sw128(q0 + qoff, 16, 1024), desc_sw128(ks + koff, 16, 1024), id1, kk > 0 ? 1u : 0u);
-            }
-            tc_commit(&sm->s_full[sb]);
-            ++g1;
-            progressed = true;
-          }
+        for (int kk = 0; kk < kPanels * 4; ++kk) {
+          const uint32_t qoff = (kk >> 2) * (kH * 128) + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+          tc_mma_bf16(d, desc_sw128(q0 + qoff, 16, 1024), desc_sw128(ks + koff, 16, 1024), id1, kk > 0 ? 1u : 0u);
         }
-        if (progressed) {
-          t_idle = 0;
-        } else {
-          const unsigned long long now = global_timer_ns();
-          if (t_idle == 0) {
-            t_idle = now;
-          } else if (*abort_flag) {
-            ok = false;
-          } else if (now - t_idle > kWaitLimitNs) {
-            raise_error(kErrTimeout);
-            *abort_flag = 1;
-            ok = false;
-          }
-        }
+        tc_commit(&sm->s_full[sb]);
       }
       tc_commit(&sm->mma_done);
       mbar_wait_drain(&sm->mma_done, 0, kWaitLimitNs);
@@ -523,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
     float m_ref = -INFINITY, l = 0.0f;
     bool all_ok = true;
+    bool gemm2_issued = false, gemm2_failed = false;  // first softmax warp, lane 0: GEMM 2 issue
     // validity of window j's keys (bit k of word h = key 32h + k), from the
     // index set itself; slots are loaded two windows ahead, checked when used
     auto load_slot = [&](int j, int h) -> int {
@@ -581,6 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (ok && j > 0) ok = warp_wait(&sm->p_free, static_cast<uint32_t>(j - 1) & 1u, abort_flag);
+      if (gemm2_failed) ok = false;
       const unsigned any_need = __ballot_sync(0xffffffffu, need);
       if (owner) sm->xa[j & 1][head] = alpha;
       if (lane == 0) {
@@ -623,6 +591,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->p_full);
+      if (w4 == 0) {
+        // GEMM 2 of window j once every softmax warp has written its P rows:
+        // O^T[512 dims, 64 heads] += V^T . P^T, then the window's stages and
+        // the P buffer are released as these MMAs complete
+        int issued = 1;
+        if (lane == 0) {
+          issued = mbar_wait_bounded(&sm->p_full, static_cast<uint32_t>(j) & 1u, abort_flag) ? 1 : 0;
+          if (issued) {
+            tc_fence_after();
+            constexpr uint32_t id2 = idesc(128, 64, true, false);
+            const uint32_t ks = smem_u32(sK) + (j % kWindows) * kKeys * 128;
+            const uint32_t p0 = smem_u32(sP);
+#pragma unroll
+            for (int c = 0; c < kDv / 128; ++c) {
+#pragma unroll
+              for (int kk = 0; kk < kKeys / 16; ++kk) {
+                const uint64_t ad = desc_sw128(ks + 2 * c * kPanelBytes + kk * 16 * 128, kPanelBytes, 1024);
+                const uint64_t bd = desc_sw128(p0 + kk * 32, 16, 1024);
+                tc_mma_bf16(tmem_base + kOCol + c * 64, ad, bd, id2, (j > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            for (int h = 0; h < kWinStages; ++h) tc_commit(&sm->empty[(j % kWindows) * kWinStages + h]);
+            tc_commit(&sm->p_free);
+            gemm2_issued = true;
+          }
+        }
+        // a failed wait fails this warp's status at the next window's barrier
+        if (!__shfl_sync(0xffffffffu, issued, 0)) gemm2_failed = true;
+      }
+    }
+    if (gemm2_issued) {
+      // every GEMM 2 this thread issued is complete before tensor memory is
+      // freed, whatever path the loop took
+      tc_commit(&sm->mma2_done);
+      mbar_wait_drain(&sm->mma2_done, 0, kWaitLimitNs);
     }
 
     // ---- epilogue: O^T / l per head, staged in the idle gather buffers
