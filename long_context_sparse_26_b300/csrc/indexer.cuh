@@ -483,18 +483,20 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
             tmem_ld_32x32b_x32_nowait(taddr, v0);
             tmem_ld_32x32b_x32_nowait(taddr + 32, v1);
             tmem_wait_ld();
-            float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent chains
+            // four independent chains of paired FMAs (two heads each)
+            float2 a[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
 #pragma unroll
             for (int j = 0; j < 64; j += 4) {
               const float4 wv = w4[j >> 2];
               const uint32_t *v = j < 32 ? v0 + j : v1 + (j - 32);
               const int c = (j >> 2) & 1;
-              a[4 * c + 0] = fmaf(wv.x, fmaxf(__uint_as_float(v[0]), 0.0f), a[4 * c + 0]);
-              a[4 * c + 1] = fmaf(wv.y, fmaxf(__uint_as_float(v[1]), 0.0f), a[4 * c + 1]);
-              a[4 * c + 2] = fmaf(wv.z, fmaxf(__uint_as_float(v[2]), 0.0f), a[4 * c + 2]);
-              a[4 * c + 3] = fmaf(wv.w, fmaxf(__uint_as_float(v[3]), 0.0f), a[4 * c + 3]);
+              a[2 * c] = ffma2(make_float2(fmaxf(__uint_as_float(v[0]), 0.0f), fmaxf(__uint_as_float(v[1]), 0.0f)),
+                               make_float2(wv.x, wv.y), a[2 * c]);
+              a[2 * c + 1] = ffma2(make_float2(fmaxf(__uint_as_float(v[2]), 0.0f), fmaxf(__uint_as_float(v[3]), 0.0f)),
+                                   make_float2(wv.z, wv.w), a[2 * c + 1]);
             }
-            s = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+            s = ((a[0].x + a[0].y) + (a[1].x + a[1].y)) + ((a[2].x + a[2].y) + (a[3].x + a[3].y));
           }
         }
         if (F8 && real && key < p.T) s *= kscale;
