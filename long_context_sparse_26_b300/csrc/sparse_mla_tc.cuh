@@ -24,7 +24,10 @@
 //           operand bytes per MMA; the ring keeps several stages in flight;
 //   softmax one thread per head reads its S row from tensor memory: masked,
 //           scaled (log2 e folded in), exponentiated against a per-head
-//           reference max, row-summed, and written as bf16 P^T rows;
+//           reference max, row-summed, and written as bf16 P^T rows into
+//           the window's own RoPE panel (dead once GEMM 1 has read it), so
+//           each window has its own P and the softmax of the next window
+//           never waits for this window's GEMM 2;
 //   GEMM 2  O^T[512 dims, 64 heads] += V^T . P^T  tcgen05, M = 128 (4 chunks of
 //           128 dims), N = 64, K = kKeys; V^T is read from the gathered
 //           panels 0..7 as an MN-major operand (no transpose pass).
@@ -76,7 +79,6 @@ constexpr int kPanels = 9;                           // 576 dims / 64
 constexpr int kPanelBytes = kRingRows * 128;         // one 64-dim panel of the ring: 16 KB
 constexpr int kRingBytes = kPanels * kPanelBytes;    // 147456
 constexpr int kQBytes = kPanels * kH * 128;          // 73728
-constexpr int kPBytes = kH * 128;                    // 64 heads x 64 keys bf16
 constexpr int kProducerWarps = 7;
 constexpr int kMmaWarp = kProducerWarps;
 constexpr int kSoftmaxWarp0 = kProducerWarps + 1;
@@ -85,7 +87,7 @@ constexpr int kTmemCols = 512;
 constexpr int kOCol = 0;
 constexpr int kSCol = 256;
 constexpr int kSmallBytes = 1024;
-constexpr int kSmemBytes = 1024 + kQBytes + kRingBytes + kPBytes + kSmallBytes;
+constexpr int kSmemBytes = 1024 + kQBytes + kRingBytes + kSmallBytes;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 static_assert(kRingBytes >= kH * kDv * 4, "the epilogue stages an fp32 partial in the gather ring");
 static_assert(kKeys % kStageRows == 0 && kStages % kWinStages == 0 && kKeys % 32 == 0, "windows tile the ring");
@@ -215,8 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sQ = base;                                  // [9 panels][64 heads][128 B]
   uint8_t *sK = sQ + kQBytes;                          // [9 panels][128 ring rows][128 B]
-  uint8_t *sP = sK + kRingBytes;                       // [64 heads][128 B]: P^T, K-major
-  Small *sm = reinterpret_cast<Small *>(sP + kPBytes);
+  Small *sm = reinterpret_cast<Small *>(sK + kRingBytes);
   volatile int *abort_flag = &sm->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -489,7 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
     float m_ref = -INFINITY, l = 0.0f;
     bool all_ok = true;
-    bool gemm2_issued = false, gemm2_failed = false;  // first softmax warp, lane 0: GEMM 2 issue
+    bool gemm2_issued = false;  // first softmax warp, lane 0: GEMM 2 issued
+    bool late_fail = false;     // a wait failed after this window's status exchange
     // validity of window j's keys (bit k of word h = key 32h + k), from the
     // index set itself; slots are loaded two windows ahead, checked when used
     auto load_slot = [&](int j, int h) -> int {
@@ -547,8 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[e] = pack_bf16x2(a, bq);
         }
       }
-      if (ok && j > 0) ok = warp_wait(&sm->p_free, static_cast<uint32_t>(j - 1) & 1u, abort_flag);
-      if (gemm2_failed) ok = false;
+      if (late_fail) ok = false;
       const unsigned any_need = __ballot_sync(0xffffffffu, need);
       if (owner) sm->xa[j & 1][head] = alpha;
       if (lane == 0) {
@@ -559,7 +560,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       all_ok = sm->status[j & 1][0] && sm->status[j & 1][1] && sm->status[j & 1][2] && sm->status[j & 1][3];
       if (!all_ok) break;
       const bool rescale = sm->need[j & 1][0] || sm->need[j & 1][1] || sm->need[j & 1][2] || sm->need[j & 1][3];
-      if (rescale && j > 0) {
+      // P needs no wait for the previous window's GEMM 2: each window writes
+      // its own P (below).  Only a rescale of O^T waits for that GEMM 2 (its
+      // phase is the latest one: GEMM 2 of this window is not issued yet).  A
+      // failed wait skips the rescale and fails this warp at the next
+      // window's barrier (or at the epilogue's), where every warp stops.
+      if (rescale && j > 0 && !warp_wait(&sm->p_free, static_cast<uint32_t>(j - 1) & 1u, abort_flag))
+        late_fail = true;
+      if (rescale && j > 0 && !late_fail) {
         // O^T column h *= alpha[h] on this warp's 32 lanes of every chunk
         // (rare: 8 columns at a time keeps the registers of the hot path free)
         tc_fence_after();
@@ -580,7 +588,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
       }
       if (owner) {
-        uint8_t *prow = sP + head * 128;
+        // P^T row `head` goes to the window's own RoPE panel (panel 8 of its
+        // ring slot): GEMM 1 of this window, its only reader, has completed,
+        // and the slot is not refilled before GEMM 2 of this window has read it
+        uint8_t *prow = sK + 8 * kPanelBytes + (j % kWindows) * kKeys * 128 + head * 128;
 #pragma unroll
         for (int c = 0; c < kKeys / 8; ++c)
           *reinterpret_cast<uint4 *>(prow + ((c ^ (head & 7)) << 4)) =
@@ -593,8 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sm->p_full);
       if (w4 == 0) {
         // GEMM 2 of window j once every softmax warp has written its P rows:
-        // O^T[512 dims, 64 heads] += V^T . P^T, then the window's stages and
-        // the P buffer are released as these MMAs complete
+        // O^T[512 dims, 64 heads] += V^T . P^T, then the window's stages
+        // (which hold its P) are released as these MMAs complete
         int issued = 1;
         if (lane == 0) {
           issued = mbar_wait_bounded(&sm->p_full, static_cast<uint32_t>(j) & 1u, abort_flag) ? 1 : 0;
@@ -602,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             constexpr uint32_t id2 = idesc(128, 64, true, false);
             const uint32_t ks = smem_u32(sK) + (j % kWindows) * kKeys * 128;
-            const uint32_t p0 = smem_u32(sP);
+            const uint32_t p0 = smem_u32(sK) + 8 * kPanelBytes + (j % kWindows) * kKeys * 128;  // P^T
 #pragma unroll
             for (int c = 0; c < kDv / 128; ++c) {
 #pragma unroll
@@ -618,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // a failed wait fails this warp's status at the next window's barrier
-        if (!__shfl_sync(0xffffffffu, issued, 0)) gemm2_failed = true;
+        if (!__shfl_sync(0xffffffffu, issued, 0)) late_fail = true;
       }
     }
     if (gemm2_issued) {
@@ -629,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- epilogue: O^T / l per head, staged in the idle gather buffers
-    bool ok = all_ok;
+    bool ok = all_ok && !late_fail;
     if (nblk > 0 && ok) ok = warp_wait(&sm->p_free, static_cast<uint32_t>(nblk - 1) & 1u, abort_flag);
     float *inv_l = sm->xa[0];
     named_bar_sync(1, 128);  // every warp is past its last read of xa
