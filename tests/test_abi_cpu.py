@@ -110,3 +110,29 @@ def test_paged_validation_rejects_before_launch(L):
                                        None, None, 0, None) == 3
     assert L.dsa_indexer_scores_paged(ctypes.byref(cfg), vp[0], vp[1], vp[2], None, vp[3], 1, 1, 100, vp[4],
                                       None) == 1     # no block table
+
+
+def test_fp8_validation_rejects_before_launch(L):
+    """The FP8 entry points check their extra arguments on the host first."""
+    cfg = binding.default_config()
+    n = None
+    vp = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(8)]
+    odd = ctypes.c_void_p(0x1004)
+    # indexer: q_idx8, q_scale, w, k_idx8, k_scale, q_pos, B, Q, T, scores, stream
+    assert L.dsa_indexer_scores_fp8(ctypes.byref(cfg), vp[0], n, vp[1], vp[2], vp[3], vp[4], 1, 1, 64, vp[5], n) == 1
+    assert L.dsa_indexer_scores_fp8(ctypes.byref(cfg), vp[0], vp[1], vp[2], vp[3], odd, vp[4], 1, 1, 64, vp[5], n) == 3
+    assert L.dsa_indexer_scores_fp8(ctypes.byref(cfg), n, n, n, n, n, n, 0, 1, 64, n, n) == 0
+    # FP8 latent attention: q, kv8, idx, B, Q, T, out, lse, ws, ws_bytes, stream
+    assert L.dsa_sparse_mla_attn_fp8(ctypes.byref(cfg), vp[0], n, vp[1], 1, 1, 64, vp[2], n, n, 0, n) == 1
+    assert L.dsa_sparse_mla_attn_fp8(ctypes.byref(cfg), vp[0], odd, vp[1], 1, 1, 64, vp[2], n, n, 0, n) == 3
+    assert L.dsa_sparse_mla_attn_fp8(ctypes.byref(cfg), n, n, n, 1, 0, 64, n, n, n, 0, n) == 0
+    # groups: the scales are checked, then the layer count
+    layers = (ctypes.c_void_p * 1)(0x9000)
+    for fn in (L.dsa_indexshare_group_forward_fp8, L.dsa_indexshare_group_forward_fp8kv):
+        assert fn(ctypes.byref(cfg), vp[0], n, vp[1], vp[2], vp[3], vp[4], layers, layers, 1, 1, 1, 64, layers,
+                  n, n, 0, n) == 1                       # no query scales
+        assert fn(ctypes.byref(cfg), vp[0], vp[1], vp[2], vp[3], odd, vp[4], layers, layers, 1, 1, 1, 64, layers,
+                  n, n, 0, n) == 3                       # misaligned key scales
+        assert fn(ctypes.byref(cfg), vp[0], vp[1], vp[2], vp[3], vp[5], vp[4], layers, layers, 9, 1, 1, 64, layers,
+                  n, n, 0, n) == 1                       # 9 layers > 8
+        assert fn(ctypes.byref(cfg), n, n, n, n, n, n, n, n, 4, 0, 1, 64, n, n, n, 0, n) == 0
