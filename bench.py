@@ -12,7 +12,13 @@ query token each).
 
 Prints one JSON line on rank 0.  Under torchrun every rank runs its own batch
 (weak scaling, no collective on the data path); the step time is the max over
-ranks.
+ranks.  After the headline workload the same run measures the other
+configurations (128K decode, chunked prefill, MTP drafting, the tiny decode
+and multi-token verification) and reports each under "workloads"
+(--only-headline skips them).  Every workload carries its step time, the
+roofline of its dominant kernel, each kernel of the path timed alone
+("kernels"), the end-to-end rate through the C ABI with host buffers and the
+clock record of its timed window.
 """
 from __future__ import annotations
 
@@ -70,9 +76,10 @@ def indexer_flops(w: wl.Workload, B: int) -> int:
 
 class ClockSampler:
     """Samples SM clocks and clock-event reasons with nvidia-smi (read-only)
-    every 100 ms in a background process."""
+    every 100 ms in a background process, for the whole run; each timed
+    window is summarised from the samples whose timestamps fall inside it."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -81,7 +88,7 @@ class ClockSampler:
         import tempfile
         fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
         os.close(fd)
-        self.t_start = time.perf_counter()
+        self.rows = None
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
@@ -91,26 +98,37 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
-        if self.proc is not None:
+        if self.proc is not None and self.rows is None:
             self.proc.terminate()
             self.proc.wait()
             self.f.close()
+            import datetime
+            self.rows = []
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        continue
+                    self.rows.append([ts] + parts[1:])
+            os.unlink(self.path)
 
     def summary(self, t0: float, t1: float) -> dict:
-        """Samples taken between t0 and t1 (perf_counter), counting ~100 ms per sample from the start."""
+        """Samples taken between wall times t0 and t1 (time.time()); the
+        nearest sample when none falls inside (windows shorter than 100 ms)."""
+        self.stop()
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        os.unlink(self.path)
+        rows = self.rows
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        lo, hi = int((t0 - self.t_start) / 0.1), int((t1 - self.t_start) / 0.1) + 1
-        inside = rows[max(0, lo):max(lo + 1, hi)] or rows
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        if not inside:
+            mid = 0.5 * (t0 + t1)
+            inside = [min(rows, key=lambda r: abs(r[0] - mid))]
 
         def num(x):
             try:
@@ -118,15 +136,15 @@ class ClockSampler:
             except ValueError:
                 return None
 
-        mhz = [v for v in (num(r[1]) for r in inside) if v is not None]
-        power = [v for v in (num(r[3]) for r in inside) if v is not None]
+        mhz = [v for v in (num(r[2]) for r in inside) if v is not None]
+        power = [v for v in (num(r[4]) for r in inside) if v is not None]
         reasons = set()
         for r in inside:
-            for name, val in (("hw_slowdown", r[5]), ("hw_thermal_slowdown", r[6]), ("sw_thermal_slowdown", r[7]),
-                              ("sw_power_cap", r[8])):
+            for name, val in (("hw_slowdown", r[6]), ("hw_thermal_slowdown", r[7]), ("sw_thermal_slowdown", r[8]),
+                              ("sw_power_cap", r[9])):
                 if val.lower() == "active":
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": num(rows[0][2]),
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": num(rows[0][3]),
                 "reasons": sorted(reasons), "samples": len(inside), "power_w_max": max(power) if power else None}
 
 
@@ -200,39 +218,41 @@ def barrier(world: int):
 
 # --------------------------------------------------------------------------- CPU oracle sample
 
-class LazyRows:
-    """Indexable view of one sequence's device latent cache: kv[positions] is
-    copied to the host as fp64 only for the positions asked for."""
-
-    def __init__(self, kv_seq: torch.Tensor):
-        self.kv = kv_seq
-
-    def __getitem__(self, pos):
-        import oracle
-        rows = self.kv[torch.as_tensor(np.asarray(pos), device=self.kv.device)].cpu()
-        return oracle.bf16_bits_to_f64(rows.contiguous().view(torch.int16).numpy().view(np.uint16))
+def _bits(x: torch.Tensor) -> np.ndarray:
+    return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
 def oracle_sample(w: wl.Workload, inp: wl.Inputs, b: int, t: int) -> float:
     """Times the oracle on one query token of sequence b: the full indexer row,
-    the stable sort, and every attention layer (or draft step).  Returns seconds."""
+    the stable sort, and every attention layer (or draft step).  Returns the
+    seconds of oracle arithmetic only: the inputs are copied to the host
+    before the clock starts, and the latent rows the oracle's own index set
+    names are fetched from the device between the two timed parts (the 1M
+    caches never fit the host), outside the clock."""
     import oracle
-    bits = lambda x: x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
-    qi, kk = bits(inp.q_idx[b, t]), bits(inp.k_idx[b])
+    qi = oracle.bf16_bits_to_f64(_bits(inp.q_idx[b, t]))
+    kk = oracle.bf16_bits_to_f64(_bits(inp.k_idx[b]))
     wv = inp.w[b, t].detach().cpu().double().numpy()
     pos = int(inp.q_pos[b, t])
     if w.kind == "mtp":
-        qs = [bits(inp.q_steps[s, b]) for s in range(w.mtp_steps)]
-        kvs = [LazyRows(inp.kv[0][b])] * w.mtp_steps
+        qs = [oracle.bf16_bits_to_f64(_bits(inp.q_steps[s, b])) for s in range(w.mtp_steps)]
+        kv_seqs = [inp.kv[0][b]] * w.mtp_steps
     else:
-        qs = [bits(q[b, t]) for q in inp.q]
-        kvs = [LazyRows(kv[b]) for kv in inp.kv]
+        qs = [oracle.bf16_bits_to_f64(_bits(q[b, t])) for q in inp.q]
+        kv_seqs = [kv[b] for kv in inp.kv]
     t0 = time.perf_counter()
-    S = oracle.indexer_scores_row(oracle.bf16_bits_to_f64(qi), wv, oracle.bf16_bits_to_f64(kk), pos)
+    S = oracle.indexer_scores_row(qi, wv, kk, pos)
     idx = oracle.topk_select_row(S, pos, w.topk)
-    for q, kv in zip(qs, kvs):
-        oracle.sparse_mla_attn_row(oracle.bf16_bits_to_f64(q), kv, idx, wl.SM_SCALE)
-    return time.perf_counter() - t0
+    t1 = time.perf_counter()
+    valid = idx[idx >= 0]
+    sel = torch.as_tensor(valid, device=inp.k_idx.device)
+    rows = [oracle.bf16_bits_to_f64(_bits(kv[sel])) for kv in kv_seqs]   # untimed data copy
+    local = np.arange(valid.shape[0])
+    t2 = time.perf_counter()
+    for q, r in zip(qs, rows):
+        oracle.sparse_mla_attn_row(q, r, local, wl.SM_SCALE)
+    t3 = time.perf_counter()
+    return (t1 - t0) + (t3 - t2)
 
 
 def cpu_info() -> dict:
@@ -272,12 +292,81 @@ def cpu_baseline(w: wl.Workload, inp: wl.Inputs, budget_s: float = 20.0) -> dict
 
 # --------------------------------------------------------------------------- GPU arm
 
-def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | None:
+L2_BYTES = 126 * 2 ** 20
+NOMINAL_HBM_GBS = 8000.0   # the "about 8 TB/s" decode yardstick of the target
+
+
+def attention_flops(w: wl.Workload, B: int) -> int:
+    """2 x 64 heads x (576 + 512) FLOPs per (query row, selected key) and layer or draft step."""
+    uses = w.mtp_steps if w.kind == "mtp" else w.n_layers
+    return uses * B * w.Q * w.topk * 2 * wl.N_HEADS * (wl.D_QK + wl.D_V)
+
+
+def input_bytes(inp: wl.Inputs) -> int:
+    ts = [inp.q_idx, inp.w, inp.k_idx, inp.q_pos] + list(inp.q or []) + list(inp.kv or [])
+    if inp.q_steps is not None:
+        ts.append(inp.q_steps)
+    return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+
+def read_stream_gbs(dev) -> float:
+    """A read-only HBM stream, for context beside the copy peak: the best of
+    10 fp32-accumulated sums over 4 GiB of bf16 (torch's reduction), timed
+    with CUDA events."""
+    x = torch.ones(2 ** 31, dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    best = 0.0
+    for _ in range(12):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        x.sum(dtype=torch.float32)
+        e1.record()
+        e1.synchronize()
+        best = max(best, x.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del x
+    torch.cuda.empty_cache()
+    return best
+
+
+def time_launches(fn, stream, n: int) -> float:
+    """Mean device time (ms) of n back-to-back launches of fn on `stream`, after 3 untimed ones."""
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(n):
+            fn()
+    e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def roofline_of(kernel: str, ms: float, nbytes: int, flops: int, hbm_gbs: float, tf_peak: float, peak_src: str,
+                tf_src: str, traffic) -> dict:
+    """The bound whose peak time is longer (bytes at the HBM peak, or FLOPs at
+    the tensor peak), and the kernel's achieved rate against it."""
+    t_bytes = nbytes / (hbm_gbs * 1e9)
+    t_flops = flops / (tf_peak * 1e12)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    tfs = flops / (ms / 1e3) / 1e12
+    if t_flops > t_bytes:
+        return {"bound": "tensor", "achieved": tfs, "peak": tf_peak, "unit": "TFLOP/s", "frac": tfs / tf_peak,
+                "traffic": traffic, "kernel": kernel, "kernel_ms": ms, "algorithmic_flops": flops,
+                "algorithmic_bytes": nbytes, "achieved_gbs": gbs, "peak_source": tf_src}
+    return {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gbs / hbm_gbs,
+            "traffic": traffic, "kernel": kernel, "kernel_ms": ms, "algorithmic_bytes": nbytes,
+            "algorithmic_flops": flops, "achieved_tflops": tfs, "peak_source": f"{peak_src} hbm copy"}
+
+
+def run_ours(args, w: wl.Workload, world: int, rank: int, local: int, clocks, headline: bool = True) -> dict | None:
+    """Measures one workload: the whole step captured in a CUDA graph and
+    timed with events (max over ranks), each kernel of the path timed alone,
+    the step end to end through the C ABI with host buffers, and (headline
+    only) the per-layer-indexer variant and the CPU oracle."""
     from long_context_sparse_26_b300 import binding as dsa
-    from long_context_sparse_26_b300.build import build_library
-    if rank == 0 or not os.path.exists(os.path.join(ROOT, "long_context_sparse_26_b300", "libdsa.so")):
-        build_library()
-    barrier(world)
     dev = f"cuda:{local}"
     torch.cuda.set_device(local)
     cfg = dsa.default_config(topk=w.topk)
@@ -288,6 +377,7 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
     ws = dsa.alloc_workspace(cfg, B, Q, T, n_att, dev)
     scores = torch.empty(B, Q, T, device=dev)
     idx = torch.empty(B, Q, w.topk, dtype=torch.int32, device=dev)
+    fp8, paged = bool(args.fp8_indexer) and w.kind != "mtp", bool(args.paged) and w.kind != "mtp"
     if w.kind == "mtp":
         out = torch.empty(w.mtp_steps, B, 64, 512, dtype=torch.bfloat16, device=dev)
         outs = [out]
@@ -296,7 +386,7 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
             dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, stream)
             dsa.topk_select(cfg, scores, inp.q_pos, idx, ws, stream)
             dsa.mtp_draft_attn(cfg, idx, inp.q_steps, inp.kv[0], out, ws, stream)
-    elif args.fp8_indexer:
+    elif fp8:
         # FP8 (E4M3) indexer caches with one fp32 scale per row; bf16 latents,
         # or FP8 latent rows too (--fp8-kv)
         q8, q_scale = wl.to_e4m3_rows(inp.q_idx)
@@ -314,7 +404,7 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
             def step():
                 dsa.indexshare_group_forward_fp8(cfg, q8, q_scale, inp.w, k8, k_scale, inp.q_pos, inp.q, inp.kv,
                                                  outs, idx, ws, stream)
-    elif args.paged:
+    elif paged:
         # the caches laid out in pages of args.paged rows, in a random page order
         pools, table = wl.paginate([inp.k_idx] + inp.kv, args.paged, seed=w.seed)
         inp.k_idx, inp.kv = None, None
@@ -332,6 +422,10 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
             dsa.indexshare_group_forward(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, inp.q, inp.kv, outs, idx,
                                          ws, stream)
 
+    # inputs under two L2 sizes would be served from L2 across steps: write a
+    # buffer larger than L2 between timed steps (outside the timed intervals)
+    flush = None if input_bytes(inp) > 2 * L2_BYTES else torch.empty(2 * L2_BYTES // 4, dtype=torch.int32,
+                                                                        device=dev)
     torch.cuda.synchronize()
     # capture one step in a CUDA graph (launch overhead off the critical path)
     with torch.cuda.stream(stream):
@@ -345,123 +439,133 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int) -> dict | 
     if status != 0:
         raise RuntimeError(f"device error before timing: {dsa.status_string(status)}")
 
-    vis = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
-    clocks = ClockSampler(vis[local] if local < len(vis) else local)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             graph.replay()
     stream.synchronize()
     # untimed load so the clock record holds samples taken under this load
-    t_settle = time.perf_counter()
+    t_settle = time.time()
     with torch.cuda.stream(stream):
-        while time.perf_counter() - t_settle < args.settle:
+        while time.time() - t_settle < args.settle:
             for _ in range(20):
                 graph.replay()
             stream.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    t_wall0 = time.perf_counter()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e_all0, e_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        ev[0].record(stream)
+        e_all0.record(stream)
         for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(i)
+            ev[i][0].record(stream)
             graph.replay()
-            ev[i + 1].record(stream)
+            ev[i][1].record(stream)
+        e_all1.record(stream)
     stream.synchronize()
-    t_wall1 = time.perf_counter()
+    t_wall1 = time.time()
     torch.cuda.synchronize()
     barrier(world)
-    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms) if flush is not None else e_all0.elapsed_time(e_all1)
     total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
     status = dsa.get_device_error(stream)
     if status != 0:
         raise RuntimeError(f"device error during timing: {dsa.status_string(status)}")
+    clk = clocks.summary(t_settle, t_wall1) if clocks is not None else None
 
-    # ---- the dominant kernel alone: indexer scores, timed with events on its stream
+    # ---- each kernel of the path alone, timed with events on its own stream
     kst = torch.cuda.Stream(device=dev)
+    n_k = max(5, min(50, args.steps))
 
     def indexer_alone():
-        if args.fp8_indexer and w.kind != "mtp":
+        if fp8:
             dsa.indexer_scores_fp8(cfg, q8, q_scale, inp.w, k8, k_scale, inp.q_pos, scores, kst)
-        elif args.paged and w.kind != "mtp":
+        elif paged:
             dsa.indexer_scores_paged(cfg, inp.q_idx, inp.w, k_pool, table, inp.q_pos, scores, kst)
         else:
             dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores, kst)
 
-    with torch.cuda.stream(kst):
-        for _ in range(3):
-            indexer_alone()
-    kst.synchronize()
-    kev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    n_k = max(5, min(50, args.steps))
-    kev[0].record(kst)
-    for _ in range(n_k):
-        indexer_alone()
-    kev[1].record(kst)
-    kst.synchronize()
-    clocks.stop()
-    idx_ms = kev[0].elapsed_time(kev[1]) / n_k
+    idx_ms = time_launches(indexer_alone, kst, n_k)
+    topk_ms = time_launches(lambda: dsa.topk_select(cfg, scores, inp.q_pos, idx, ws, kst), kst, n_k)
+    attn_ms = None
+    if w.kind == "mtp":
+        attn_ms = time_launches(lambda: dsa.mtp_draft_attn(cfg, idx, inp.q_steps, inp.kv[0], out, ws, kst), kst, n_k)
+    elif not fp8 and not paged:
+        attn_ms = time_launches(lambda: dsa.sparse_mla_attn_shared(cfg, inp.q, inp.kv, idx, outs, ws, kst), kst, n_k)
+    status = dsa.get_device_error(kst)
+    if status != 0:
+        raise RuntimeError(f"device error in the kernel timings: {dsa.status_string(status)}")
 
     hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = measured_peaks()
-    alg = algorithmic_bytes(w, B, fp8_keys=bool(args.fp8_indexer), fp8_kv=bool(args.fp8_kv))
+    alg = algorithmic_bytes(w, B, fp8_keys=fp8, fp8_kv=bool(args.fp8_kv))
     flops = indexer_flops(w, B)
     tokens = B * Q * world if w.kind != "mtp" else B * w.mtp_steps * world
     value = tokens / (ms_per_step / 1e3)
-    idx_gbs = alg["indexer_keys"] / (idx_ms / 1e3) / 1e9
-    idx_tfs = flops / (idx_ms / 1e3) / 1e12
-    # the indexer is bound by its key stream or by its tensor work, whichever
-    # takes longer at peak (a few queries per sequence: keys; many: FLOPs).
     # FP8 operands: the measured bf16 peak times the nominal E4M3:bf16 dense
     # ratio (4.5 / 2.25 PFLOP/s)
-    mma_tf = bf16_tf * (2.0 if args.fp8_indexer else 1.0)
-    mma_src = f"{peak_src} bf16 burst" + (" x 2 (nominal e4m3:bf16 dense ratio)" if args.fp8_indexer else "")
-    tensor_bound = flops / (mma_tf * 1e12) > alg["indexer_keys"] / (hbm_gbs * 1e9)
-    if tensor_bound:
-        qg = 1 if Q == 1 else (2 if Q == 2 else 4)
-        roof = {"bound": "tensor", "achieved": idx_tfs, "peak": mma_tf, "unit": "TFLOP/s", "frac": idx_tfs / mma_tf,
-                "traffic": profiled_traffic("indexer.cuh", w.name + (":fp8" if args.fp8_indexer else "")), "kernel": f"indexer_scores_kernel<{qg}>",
-                "kernel_ms": idx_ms, "algorithmic_flops": flops, "peak_source": mma_src}
-    else:
-        qg = 1 if Q == 1 else (2 if Q == 2 else 4)
-        roof = {"bound": "hbm", "achieved": idx_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": idx_gbs / hbm_gbs,
-                "traffic": profiled_traffic("indexer.cuh", w.name + (":fp8" if args.fp8_indexer else "")), "kernel": f"indexer_scores_kernel<{qg}>",
-                "kernel_ms": idx_ms, "algorithmic_bytes": alg["indexer_keys"], "peak_source": f"{peak_src} hbm copy"}
+    mma_tf = bf16_tf * (2.0 if fp8 else 1.0)
+    mma_src = f"{peak_src} bf16 burst" + (" x 2 (nominal e4m3:bf16 dense ratio)" if fp8 else "")
+    qg = 1 if Q == 1 else (2 if Q == 2 else 4)
+    kernels = {
+        "indexer": roofline_of(f"indexer_scores_kernel<{qg}>", idx_ms, alg["indexer_keys"], flops, hbm_gbs, mma_tf,
+                               peak_src, mma_src,
+                               profiled_traffic("indexer.cuh", w.name + (":fp8" if fp8 else ""))),
+        "topk": {"kernel": "topk (standalone call: histogram, scan and select launches)", "kernel_ms": topk_ms,
+                 "note": "inside the group at one query per sequence the histogram is counted by the indexer"},
+    }
+    if attn_ms is not None:
+        kernels["attention"] = roofline_of(
+            "sparse_mla_tc_kernel + combine", attn_ms, alg["gathered_rows"], attention_flops(w, B), hbm_gbs, bf16_tf,
+            peak_src, f"{peak_src} bf16 burst", profiled_traffic("sparse_mla_tc.cuh", w.name))
+    dominant = max((k for k in ("indexer", "attention") if k in kernels), key=lambda k: kernels[k]["kernel_ms"])
+    roof = dict(kernels[dominant])
+    if roof["bound"] == "hbm":
+        roof["frac_of_nominal_8tbs"] = roof["achieved"] / NOMINAL_HBM_GBS
+        if args.read_peak_gbs:
+            roof["read_stream_gbs"] = args.read_peak_gbs
+            roof["frac_of_best_hbm_peak"] = roof["achieved"] / max(args.read_peak_gbs, hbm_gbs)
     step_gbs = alg["total"] / (ms_per_step / 1e3) / 1e9
-    step_roof = {"algorithmic_bytes": alg["total"], "achieved_gbs": step_gbs, "frac_of_measured_hbm": step_gbs / hbm_gbs,
-                 "frac_of_nominal_8tbs": step_gbs / 8000.0, "roofline_ms": alg["total"] / (hbm_gbs * 1e9) * 1e3}
-    if tensor_bound:
-        t_flops = flops / (mma_tf * 1e12) * 1e3
-        step_roof["roofline_ms"] = max(step_roof["roofline_ms"], t_flops)
-        step_roof["frac_of_roofline_time"] = step_roof["roofline_ms"] / ms_per_step
+    step_roof = {"algorithmic_bytes": alg["total"], "achieved_gbs": step_gbs,
+                 "frac_of_measured_hbm": step_gbs / hbm_gbs, "frac_of_nominal_8tbs": step_gbs / NOMINAL_HBM_GBS,
+                 "roofline_ms": alg["total"] / (hbm_gbs * 1e9) * 1e3}
+    if args.read_peak_gbs:
+        step_roof["frac_of_best_hbm_peak"] = step_gbs / max(args.read_peak_gbs, hbm_gbs)
+    t_flops = flops / (mma_tf * 1e12) * 1e3
+    if t_flops > step_roof["roofline_ms"]:
+        step_roof["roofline_ms"] = t_flops
+        step_roof["bound"] = "indexer FLOPs at the tensor peak"
+    step_roof["frac_of_roofline_time"] = step_roof["roofline_ms"] / ms_per_step
 
     # ---- end to end through the public API with host buffers
-    e2e = None if (args.no_e2e or args.paged or args.fp8_indexer) else run_e2e(args, w, cfg, inp, outs, idx, scores, ws,
-                                                                             stream, dsa)
+    e2e = None if (args.no_e2e or paged or fp8) else run_e2e(args, w, cfg, inp, outs, idx, scores, ws, stream, dsa)
 
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("fp8 e4m3 indexer and latent caches, bf16 attention math" if args.fp8_kv else
-                  "fp8 e4m3 indexer, bf16 attention") if args.fp8_indexer else "bf16", "data": "synthetic",
+                  "fp8 e4m3 indexer, bf16 attention") if fp8 else "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "Q": Q, "T": T, "topk": w.topk,
                    "layers_per_group": w.n_layers if w.kind != "mtp" else 1,
                    "mtp_steps": w.mtp_steps or None, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (no flush needed)", "graph": "one step captured, replayed",
-                   "kv_layout": f"paged, {args.paged}-row pages in random order" if args.paged else "contiguous",
-                   "indexer_cache": "fp8 e4m3 + fp32 row scales" if args.fp8_indexer else "bf16",
+                   "l2": ("L2 flushed between timed steps (inputs fit in L2)" if flush is not None
+                          else "inputs larger than L2 (no flush needed)"),
+                   "graph": "one step captured, replayed",
+                   "kv_layout": f"paged, {args.paged}-row pages in random order" if paged else "contiguous",
+                   "indexer_cache": "fp8 e4m3 + fp32 row scales" if fp8 else "bf16",
                    "latent_cache": "fp8 e4m3 + fp32 group scales, bf16 rope (656 B rows)" if args.fp8_kv else "bf16"},
-        "roofline": roof, "step_roofline": step_roof,
+        "roofline": roof, "step_roofline": step_roof, "kernels": kernels,
         "e2e": e2e,
         "gpu_launches": (launches_per_step or 0) * args.steps,
         "gpu_launches_per_step": launches_per_step,
-        "clocks": clocks.summary(t_settle, t_wall1),
+        "clocks": clk,
         "step_ms_median": statistics.median(step_ms),
     }
-    if w.name == wl.DECODE_1M.name and not args.no_variant and not args.paged and not args.fp8_indexer:
+    if headline and w.name == wl.DECODE_1M.name and not args.no_variant and not paged and not fp8:
         res["per_layer_indexer"] = run_per_layer_variant(args, w, cfg, inp, dev, ms_per_step, dsa)
-    if rank == 0 and not args.no_cpu_baseline and not args.paged and not args.fp8_indexer:
+    if headline and rank == 0 and not args.no_cpu_baseline and not paged and not fp8:
         res["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_budget)
     return res
 
@@ -677,6 +781,18 @@ def profile_kernel(args, w: wl.Workload):
         sys.exit(1)
 
 
+# The other configurations of the method, measured after the headline in the
+# same run and reported under "workloads" (each with its own step time,
+# rooflines, end-to-end rate and clock record).
+EXTRA_WORKLOADS = (wl.DECODE_128K.name, wl.PREFILL.name, wl.MTP.name, wl.TINY.name, wl.VERIFY.name)
+
+
+def summary_of(r: dict) -> dict:
+    keep = ("value", "unit", "ms_per_step", "step_ms_median", "roofline", "step_roofline", "kernels", "e2e",
+            "clocks", "gpu_launches_per_step", "config")
+    return {k: r[k] for k in keep if k in r}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -684,11 +800,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--only-headline", action="store_true",
+                    help="measure the selected workload only (no 'workloads' entries for the other configs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variant", action="store_true", help="skip the per-layer-indexer comparison")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--settle", type=float, default=1.0, help="seconds of untimed load before timing (clock record)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-read-peak", action="store_true", help="skip the read-only stream measurement")
     ap.add_argument("--batch", type=int, default=None, help="smaller batch (a small case for profiling)")
     ap.add_argument("--fp8-indexer", action="store_true",
                     help="store the indexer caches as FP8 (E4M3) rows with fp32 scales (decode workloads)")
@@ -717,7 +836,31 @@ def main():
     if args.profile_kernel:
         profile_kernel(args, w)
         return
-    res = run_ours(args, w, world, rank, local)
+    from long_context_sparse_26_b300.build import build_library
+    if rank == 0 or not os.path.exists(os.path.join(ROOT, "long_context_sparse_26_b300", "libdsa.so")):
+        build_library()
+    barrier(world)
+    torch.cuda.set_device(local)
+    vis = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    clocks = ClockSampler(vis[local] if local < len(vis) else local)
+    args.read_peak_gbs = None if args.no_read_peak else read_stream_gbs(f"cuda:{local}")
+    res = run_ours(args, w, world, rank, local, clocks, headline=True)
+    extras = not (args.only_headline or args.batch is not None or args.fp8_indexer or args.paged)
+    if extras:
+        import gc
+        settle = args.settle
+        args.settle = min(settle, 0.5)
+        res["workloads"] = {}
+        for name in EXTRA_WORKLOADS:
+            if name == w.name:
+                continue
+            gc.collect()
+            torch.cuda.empty_cache()
+            r = run_ours(args, wl.WORKLOADS[name], world, rank, local, clocks, headline=False)
+            res["workloads"][name] = summary_of(r)
+            del r
+        args.settle = settle
+    clocks.stop()
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

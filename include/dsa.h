@@ -127,13 +127,31 @@ dsa_status_t dsa_sparse_mla_attn(const dsa_config_t *cfg, const dsa_bf16_t *q, c
  *          bf16 for l < n_layers (HOST arrays of n_layers device pointers;
  *          1 <= n_layers <= 8)
  *   idx_out [B, Q, topk] int32: optional (NULL allowed) copy of the shared set
- * The index set is computed once and read by all n_layers layers. */
+ * The index set is computed once and read by all n_layers layers.  When the
+ * stream reaches the end of the call, the workspace begins with the group's
+ * indexer scores, [B, Q, T] fp32 exactly as dsa_indexer_scores writes them
+ * (the same holds for the _paged and _fp8 group entry points below). */
 dsa_status_t dsa_indexshare_group_forward(const dsa_config_t *cfg, const dsa_bf16_t *q_idx,
                                           const float *w, const dsa_bf16_t *k_idx,
                                           const int32_t *q_pos, const dsa_bf16_t *const *q,
                                           const dsa_bf16_t *const *kv, int n_layers, int B, int Q,
                                           int T, dsa_bf16_t *const *out, int32_t *idx_out, void *ws,
                                           size_t ws_bytes, dsa_stream_t stream);
+
+/* Sparse MLA attention of n_layers layers over ONE shared index set (the
+ * reuse half of step a4: the layers of an IndexShare group after the first
+ * attend over the index set the first one selected).  One launch covers every
+ * layer.
+ *   q[l] [B, Q, 64, 576] bf16, kv[l] [B, T, 576] bf16, out[l] [B, Q, 64, 512]
+ *        bf16 for l < n_layers (HOST arrays of device pointers; 1..8 layers)
+ *   idx  [B, Q, topk] int32, as for dsa_sparse_mla_attn
+ * Layer l's output equals dsa_sparse_mla_attn on (q[l], kv[l], idx) up to
+ * the rounding of a different split of the key range.  Uses the workspace
+ * (dsa_workspace_bytes with the same n_layers). */
+dsa_status_t dsa_sparse_mla_attn_shared(const dsa_config_t *cfg, const dsa_bf16_t *const *q,
+                                        const dsa_bf16_t *const *kv, int n_layers, const int32_t *idx, int B,
+                                        int Q, int T, dsa_bf16_t *const *out, void *ws, size_t ws_bytes,
+                                        dsa_stream_t stream);
 
 /* MTP draft attention with index reuse (step a6).
  *   idx0    [B, 1, topk]    int32  the step-0 index set (from the indexer and
@@ -254,6 +272,21 @@ dsa_status_t dsa_indexshare_group_forward_fp8kv(const dsa_config_t *cfg, const u
                                                 const uint8_t *const *kv8, int n_layers, int B, int Q, int T,
                                                 dsa_bf16_t *const *out, int32_t *idx_out, void *ws, size_t ws_bytes,
                                                 dsa_stream_t stream);
+
+/* Sets the time limit of the library's bounded device-side waits (an
+ * mbarrier phase a kernel waits on: a tile landing, an MMA completing, a peer
+ * warp's arrival), in nanoseconds of the GPU's global timer, for every kernel
+ * enqueued on the current device after this call; 0 restores the default of
+ * 2 s.  A kernel whose wait runs out records DSA_ERR_TIMEOUT in the device
+ * error word, stops its block in step (copies and MMAs still in flight are
+ * drained, tensor memory is freed after them), leaves its outputs
+ * unspecified and returns; the context stays usable.  The drain waits at
+ * block exit always keep the full 2 s limit.  The pages have no counterpart:
+ * this is the library's failure-detection knob, so that a caller can make a
+ * stuck dependency surface sooner than 2 s.
+ * Synchronous with respect to the host (it writes a __device__ variable);
+ * returns DSA_ERR_CUDA if that write fails. */
+dsa_status_t dsa_set_wait_limit_ns(unsigned long long limit_ns);
 
 /* Human-readable name of a status. */
 const char *dsa_status_string(dsa_status_t status);

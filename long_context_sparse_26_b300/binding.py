@@ -25,7 +25,7 @@ EXPORTS = ("dsa_config_default", "dsa_workspace_bytes", "dsa_indexer_scores", "d
            "dsa_status_string", "dsa_get_device_error", "dsa_sparse_mla_attn_noalloc",
            "dsa_indexer_scores_paged", "dsa_sparse_mla_attn_paged", "dsa_indexshare_group_forward_paged",
            "dsa_indexer_scores_fp8", "dsa_indexshare_group_forward_fp8", "dsa_sparse_mla_attn_fp8",
-           "dsa_indexshare_group_forward_fp8kv")
+           "dsa_indexshare_group_forward_fp8kv", "dsa_set_wait_limit_ns", "dsa_sparse_mla_attn_shared")
 
 FP8_LATENT_ROW_BYTES = 656  # 512 E4M3 codes, 4 fp32 group scales, 64 bf16 RoPE dims
 
@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
                                                    ctypes.POINTER(_VP), _I, _I, _I, _I, ctypes.POINTER(_VP),
                                                    _VP, _VP, _SZ, _VP]
         L.dsa_mtp_draft_attn.argtypes = [_CFG, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _SZ, _VP]
+        L.dsa_sparse_mla_attn_shared.argtypes = [_CFG, ctypes.POINTER(_VP), ctypes.POINTER(_VP), _I, _VP, _I, _I,
+                                                 _I, ctypes.POINTER(_VP), _VP, _SZ, _VP]
         L.dsa_sparse_mla_attn_noalloc.argtypes = [_CFG, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP]
         _PG = ctypes.POINTER(DsaPages)
         L.dsa_indexer_scores_paged.argtypes = [_CFG, _VP, _VP, _VP, _PG, _VP, _I, _I, _I, _VP, _VP]
@@ -90,9 +92,12 @@ def lib() -> ctypes.CDLL:
                      "dsa_sparse_mla_attn_noalloc", "dsa_indexer_scores_paged", "dsa_sparse_mla_attn_paged",
                      "dsa_indexshare_group_forward_paged", "dsa_indexer_scores_fp8",
                      "dsa_indexshare_group_forward_fp8", "dsa_sparse_mla_attn_fp8",
-                     "dsa_indexshare_group_forward_fp8kv"):
+                     "dsa_indexshare_group_forward_fp8kv", "dsa_set_wait_limit_ns",
+                     "dsa_sparse_mla_attn_shared"):
             getattr(L, name).restype = ctypes.c_int
         L.dsa_get_device_error.argtypes = [_VP]
+        L.dsa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        L.dsa_set_wait_limit_ns.restype = ctypes.c_int
         L.dsa_status_string.argtypes = [ctypes.c_int]
         L.dsa_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -206,6 +211,27 @@ def indexshare_group_forward(cfg, q_idx, w, k_idx, q_pos, qs: Sequence[torch.Ten
                                               _s(stream)), "dsa_indexshare_group_forward")
 
 
+def sparse_mla_attn_shared(cfg, qs: Sequence[torch.Tensor], kvs: Sequence[torch.Tensor], idx,
+                           outs: Sequence[torch.Tensor], ws=None, stream=None):
+    """len(qs) attention layers over one shared index set, in one launch:
+    qs[l] [B,Q,64,576] bf16, kvs[l] [B,T,576] bf16, idx [B,Q,topk] i32 -> outs[l] [B,Q,64,512] bf16."""
+    _need(idx, "idx", torch.int32, 3)
+    n = len(qs)
+    if len(kvs) != n or len(outs) != n:
+        raise ValueError("qs, kvs and outs must have one tensor per layer")
+    for i in range(n):
+        _need(qs[i], f"q[{i}]", torch.bfloat16, 4); _need(kvs[i], f"kv[{i}]", torch.bfloat16, 3)
+        _need(outs[i], f"out[{i}]", torch.bfloat16, 4)
+    B, Q, T = qs[0].shape[0], qs[0].shape[1], kvs[0].shape[1]
+    arr = _VP * n
+    qa = arr(*[t.data_ptr() for t in qs])
+    ka = arr(*[t.data_ptr() for t in kvs])
+    oa = arr(*[t.data_ptr() for t in outs])
+    _check(lib().dsa_sparse_mla_attn_shared(ctypes.byref(cfg), qa, ka, n, _p(idx), B, Q, T, oa, _p(ws),
+                                            0 if ws is None else ws.numel(), _s(stream)),
+           "dsa_sparse_mla_attn_shared")
+
+
 def mtp_draft_attn(cfg, idx0, q_steps, kv, out, ws=None, stream=None):
     """idx0 [B,1,topk] i32, q_steps [S,B,64,576] bf16, kv [B,T,576] bf16 -> out [S,B,64,512] bf16."""
     _need(idx0, "idx0", torch.int32, 3); _need(q_steps, "q_steps", torch.bfloat16, 4)
@@ -309,6 +335,11 @@ def indexshare_group_forward_fp8(cfg, q8, q_scale, w, k8, k_scale, q_pos, qs, kv
 def get_device_error(stream=None) -> int:
     """Synchronizes the stream, reads and clears the device error word; returns the status code."""
     return int(lib().dsa_get_device_error(_s(stream)))
+
+
+def set_wait_limit_ns(limit_ns: int) -> None:
+    """Time limit of the kernels' bounded device waits (0: the default 2 s)."""
+    _check(lib().dsa_set_wait_limit_ns(int(limit_ns)), "dsa_set_wait_limit_ns")
 
 
 def status_string(status: int) -> str:

@@ -1,6 +1,6 @@
 // Device-side helpers for libdsa: inline-PTX wrappers for mbarriers, TMA,
-// tcgen05 (5th-gen tensor cores + tensor memory), cp.async, ldmatrix and
-// mma.sync, plus the device error word.  sm_103a only.
+// tcgen05 (5th-gen tensor cores + tensor memory) and cp.async, plus the
+// device error word.  sm_103a only.
 #pragma once
 
 #include <cuda.h>
@@ -21,8 +21,16 @@ __device__ unsigned int g_error_word;
 
 __device__ __forceinline__ void raise_error(unsigned bits) { atomicOr(&g_error_word, bits); }
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
+// A bounded wait gives up after g_wait_limit_ns nanoseconds of %globaltimer
+// (kWaitLimitNs unless the host set another limit).  The waits that drain
+// copies and MMAs still in flight before a block exits always use the full
+// kWaitLimitNs, so a short limit never lets a block leave with work pending.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+__device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+
+__device__ __forceinline__ unsigned long long wait_limit_ns() {
+  return *static_cast<volatile unsigned long long *>(&g_wait_limit_ns);
+}
 
 __device__ __forceinline__ unsigned long long global_timer_ns() {
   unsigned long long t;
@@ -67,7 +75,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits for the phase of parity `parity` to complete.  Gives up after
-// kWaitLimitNs, or as soon as *abort is set by another thread of the block;
+// wait_limit_ns(), or as soon as *abort is set by another thread of the block;
 // on giving up it records kErrTimeout, sets *abort and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -76,7 +84,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > wait_limit_ns()) {
         raise_error(kErrTimeout);
         *abort = 1;
         return false;
@@ -254,7 +262,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32_nowait(uint32_t taddr, uint32
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
-// cp.async (16-byte, zero-filled when src_bytes == 0), ldmatrix, mma.sync
+// cp.async (16-byte, zero-filled when src_bytes == 0)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -267,27 +275,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulators.
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -230,7 +230,7 @@ Layout layout(int B, int Q, int T, int n_layers, int K, int sms) {
   const long long rows = static_cast<long long>(B) * Q;
   L.ts = topk_shape(static_cast<int>(rows), T, sms);
   size_t off = 0;
-  L.scores = off;
+  L.scores = off;  // offset 0: a group call leaves its scores at the start of the workspace (dsa.h)
   off = align_up(off + static_cast<size_t>(rows) * T * sizeof(float), 256);
   // chunked top-k: digit histograms, row plans and per-chunk candidate
   // counts (zeroed by one memset, so they are adjacent), then room for T
@@ -558,6 +558,32 @@ dsa_status_t dsa_indexshare_group_forward(const dsa_config_t *cfg, const dsa_bf1
                        reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
+dsa_status_t dsa_sparse_mla_attn_shared(const dsa_config_t *cfg, const dsa_bf16_t *const *q,
+                                        const dsa_bf16_t *const *kv, int n_layers, const int32_t *idx, int B,
+                                        int Q, int T, dsa_bf16_t *const *out, void *ws, size_t ws_bytes,
+                                        dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
+  DSA_TRY(check_sizes(B, Q, T));
+  if (n_layers < 1 || n_layers > kMaxLayers) return DSA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * Q * n_layers > kMaxRowsY) return DSA_ERR_INVALID_ARG;
+  if (!q || !kv || !out || !idx) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(idx) || (ws && !aligned16(ws))) return DSA_ERR_ALIGNMENT;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!q[l] || !kv[l] || !out[l]) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q[l]) || !aligned16(kv[l]) || !aligned16(out[l])) return DSA_ERR_ALIGNMENT;
+  }
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  const Layout L = layout(B, Q, T, n_layers, cfg->topk, dev->sms);
+  if (attn_shape(static_cast<long long>(B) * Q * n_layers, cfg->topk, dev->sms).nsplit > 1 &&
+      (ws == nullptr || ws_bytes < L.total))
+    return DSA_ERR_WORKSPACE;
+  return launch_attention(*dev, L, static_cast<uint8_t *>(ws), q, reinterpret_cast<const void *const *>(kv), out,
+                          nullptr, n_layers, idx, B * Q, Q, T, cfg->topk, cfg->sm_scale,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
 dsa_status_t dsa_mtp_draft_attn(const dsa_config_t *cfg, const int32_t *idx0, const dsa_bf16_t *q_steps,
                                 const dsa_bf16_t *kv, int S, int B, int T, dsa_bf16_t *out, void *ws, size_t ws_bytes,
                                 dsa_stream_t stream) {
@@ -813,6 +839,11 @@ const char *dsa_status_string(dsa_status_t s) {
     case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
   }
   return "DSA_ERR_UNKNOWN";
+}
+
+dsa_status_t dsa_set_wait_limit_ns(unsigned long long limit_ns) {
+  const unsigned long long v = limit_ns == 0 ? dsa::kWaitLimitNs : limit_ns;
+  return cudaMemcpyToSymbol(dsa::g_wait_limit_ns, &v, sizeof(v)) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 dsa_status_t dsa_get_device_error(dsa_stream_t stream) {

@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               t_idle = now;
             } else if (*abort_flag) {
               stop = 1;
-            } else if (now - t_idle > kWaitLimitNs) {
+            } else if (now - t_idle > wait_limit_ns()) {
               raise_error(kErrTimeout);
               *abort_flag = 1;
               stop = 1;

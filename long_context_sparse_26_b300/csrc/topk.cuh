@@ -83,10 +83,17 @@ struct Scratch {
 // count, finds the bin b with count(bins > b) < need <= count(bins >= b).
 // Writes b to sc->result[0], need - count(bins > b) to result[1] and the bin's
 // own count to result[2].  Called by every thread; ends with the result visible.
+// (If the histogram holds fewer than `need` entries, which consistent inputs
+// never give, the result is bin 0 with the whole `need` left and count 0.)
 template <int NBINS = kBins>
 __device__ void find_threshold_bin(const uint32_t *hist, uint32_t need, Scratch *sc) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   constexpr int per = NBINS / kThreads;  // bins per thread
+  if (t == 0) {
+    sc->result[0] = 0;
+    sc->result[1] = need;
+    sc->result[2] = 0;
+  }
   uint32_t h[per];
   uint32_t ts = 0;
 #pragma unroll
@@ -205,6 +212,11 @@ __device__ __forceinline__ RowPlan plan_row(const uint32_t *hist0, uint32_t K, S
 __device__ __forceinline__ RowPlan plan_row_global(const uint32_t *g, uint32_t K, Scratch *sc) {
   static_assert(kBins0 == (kThreads / 32) * 512, "one 512-bin slice per warp");
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (threadIdx.x == 0) {  // what an inconsistent histogram (fewer than K entries) leaves
+    sc->result[0] = 0;
+    sc->result[1] = K;
+    sc->result[2] = 0;
+  }
   uint32_t h[16];
   uint32_t tot = 0;
 #pragma unroll
@@ -412,7 +424,7 @@ __device__ void row_select_multipass(const float *srow, int L, int K, int32_t *o
     const uint32_t eq_rank = eq_base + block_prefix(eq, &eq_tot, sc);
     const bool sel = gt || (eq && eq_rank < need);
     const uint32_t slot = out_base + block_prefix(sel, &sel_tot, sc);
-    if (sel) out[slot] = i;
+    if (sel && slot < static_cast<uint32_t>(K)) out[slot] = i;
     out_base += sel_tot;
     eq_base += eq_tot;
   }
@@ -439,8 +451,9 @@ __device__ __forceinline__ SmemViews smem_views(uint8_t *smem) {
 }
 
 // Writes the k positions of src[0..n) (position-ordered) whose composite is >=
-// tau to out[0..k), in order: each thread takes a contiguous run.
-__device__ void write_ordered(const uint64_t *src, uint32_t n, uint64_t tau, int32_t *out, Scratch *sc) {
+// tau to out[0..k), in order: each thread takes a contiguous run.  Exactly k
+// qualify on consistent inputs; nothing is ever written past out[k - 1].
+__device__ void write_ordered(const uint64_t *src, uint32_t n, uint64_t tau, int K, int32_t *out, Scratch *sc) {
   const uint32_t per = (n + kThreads - 1) / kThreads;
   const uint32_t r0 = threadIdx.x * per;
   const uint32_t r1 = r0 + per < n ? r0 + per : n;
@@ -449,7 +462,10 @@ __device__ void write_ordered(const uint64_t *src, uint32_t n, uint64_t tau, int
   uint32_t tot;
   uint32_t off = block_exclusive_sum(mine, &tot, sc);
   for (uint32_t i = r0; i < r1; ++i)
-    if (src[i] >= tau) out[off++] = composite_pos(src[i]);
+    if (src[i] >= tau) {
+      if (off < static_cast<uint32_t>(K)) out[off] = composite_pos(src[i]);
+      ++off;
+    }
 }
 
 // Step 4 on n candidates in shared memory (position-ordered when `ordered`).
@@ -458,11 +474,10 @@ __device__ void write_ordered(const uint64_t *src, uint32_t n, uint64_t tau, int
 // inside bin b0 at composite bit 50.
 __device__ void finish_row(const uint64_t *cand, uint32_t n, int K, const RowPlan &rp, bool ordered,
                            const SmemViews &s, int32_t *out, Scratch *sc) {
-  (void)K;
   const uint64_t tau = select_threshold(cand, n, rp.need1, s.hist, sc, static_cast<uint64_t>(rp.b0) << 51,
                                         0x1FFFull << 51, 40);
   if (ordered)
-    write_ordered(cand, n, tau, out, sc);
+    write_ordered(cand, n, tau, K, out, sc);
   else
     write_sorted(cand, n, tau, K, s.sortbuf, out, sc);
 }

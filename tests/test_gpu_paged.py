@@ -1,8 +1,9 @@
 """Paged caches (fixed-size pages in a pool, one block table per sequence).
 
 A paged call reads exactly the rows its contiguous twin reads, in the same
-order, so the results must match bit for bit; the oracle ties the layout to
-its definition through gather_pages.
+order, so the results must match bit for bit.  Every paged entry point is
+also compared with the oracle over the cache its pool stands for
+(oracle.gather_pages), element by element at the parity tolerances.
 """
 import numpy as np
 import pytest
@@ -11,7 +12,7 @@ import torch
 import oracle
 from long_context_sparse_26_b300 import binding as dsa
 from long_context_sparse_26_b300 import workloads as wl
-from parity import check_scores_row, f64
+from parity import check_attention, check_scores_row, check_topk_row, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -81,6 +82,11 @@ def test_paged_attention_equals_contiguous(B, Q, T, k, page):
     dsa.sparse_mla_attn_paged(cfg, q, kv_pool, table, idx, got, T, got_lse, ws)
     torch.cuda.synchronize()
     assert torch.equal(got, ref) and torch.equal(got_lse, ref_lse)
+    # and against the oracle over the cache the pool stands for
+    kv_o = oracle.gather_pages(f64(kv_pool), table.cpu().numpy(), T)
+    O, LSE = oracle.sparse_mla_attn(f64(q), kv_o, idx.cpu().numpy(), wl.SM_SCALE)
+    check_attention(f64(got), O)
+    assert np.abs(got_lse.cpu().double().numpy() - LSE).max() < 1e-3
 
 
 @pytest.mark.parametrize("B,Q,T,page", [(3, 1, 50_000, 64), (1, 4, 9000, 128)])
@@ -103,6 +109,24 @@ def test_paged_group_equals_contiguous(B, Q, T, page):
     assert torch.equal(idx_got, idx_ref)
     for a, b in zip(outs_got, outs_ref):
         assert torch.equal(a, b)
+    # and against the oracle's group over the caches the pools stand for
+    tab = table.cpu().numpy()
+    pos = inp.q_pos.cpu().numpy()
+    k_o = oracle.gather_pages(f64(k_pool), tab, T)
+    kv_o = [oracle.gather_pages(f64(p_), tab, T) for p_ in kv_pools]
+    S = oracle.indexer_scores(f64(inp.q_idx), f64(inp.w), k_o, pos)
+    o_idx, o_outs, _ = oracle.indexshare_group_forward(f64(inp.q_idx), f64(inp.w), k_o, pos,
+                                                       [f64(q) for q in inp.q], kv_o, 2048, wl.SM_SCALE)
+    g_idx = idx_got.cpu().numpy()
+    for b in range(B):
+        for t in range(Q):
+            check_topk_row(g_idx[b, t], o_idx[b, t], S[b, t], int(pos[b, t]), 2048)
+    for layer in range(4):
+        if np.array_equal(g_idx, o_idx):
+            ref = o_outs[layer]
+        else:   # boundary ties: the oracle's attention over the GPU's index set
+            ref, _ = oracle.sparse_mla_attn(f64(inp.q[layer]), kv_o[layer], g_idx, wl.SM_SCALE)
+        check_attention(f64(outs_got[layer]), ref)
 
 
 def test_full_decode_128k_paged_equals_contiguous():
@@ -125,6 +149,25 @@ def test_full_decode_128k_paged_equals_contiguous():
     assert torch.equal(idx_got, idx_ref)
     for a, b in zip(outs_got, outs_ref):
         assert torch.equal(a, b)
+    # sampled sequences against the oracle through the pools: the key cache of
+    # sequence b and the pool row of each of its positions come from
+    # oracle.gather_pages over b's block-table row
+    tab = table.cpu().numpy()
+    page = pools[0].shape[1]
+    row_ids = np.arange(pools[0].shape[0] * page, dtype=np.int64).reshape(-1, page, 1)
+    g_idx = idx_got.cpu().numpy()
+    for b in (0, 13, 31):
+        rows_b = torch.from_numpy(oracle.gather_pages(row_ids, tab[b:b + 1], T)[0, :, 0]).to(DEV)
+        k_b = f64(pools[0].view(-1, 128)[rows_b])
+        pos = int(inp.q_pos[b, 0])
+        S = oracle.indexer_scores_row(f64(inp.q_idx[b, 0]), f64(inp.w[b, 0]), k_b, pos)
+        o_idx = oracle.topk_select_row(S, pos, 2048)
+        check_topk_row(g_idx[b, 0], o_idx, S, pos, 2048)
+        gv = torch.from_numpy(g_idx[b, 0][g_idx[b, 0] >= 0]).to(DEV)
+        for layer in range(4):
+            kv_rows = f64(pools[1 + layer].view(-1, 576)[rows_b[gv.long()]])
+            O, _ = oracle.sparse_mla_attn_row(f64(inp.q[layer][b, 0]), kv_rows, np.arange(gv.numel()), wl.SM_SCALE)
+            check_attention(f64(outs_got[layer][b, 0]), O)
     del pools, inp
     torch.cuda.empty_cache()
 

@@ -164,6 +164,22 @@ def test_sparse_attention(B, Q, T, k, pad):
     assert np.abs(lse.cpu().double().numpy() - LSE).max() < 1e-3
 
 
+def test_sparse_attention_shared_layers():
+    """Three layers over one shared index set (with padding slots) in one
+    launch, each against the oracle on its own cache."""
+    cfg = dsa.default_config(topk=1000)
+    B, Q, T, n = 2, 3, 7000, 3
+    _, _, idx = _attn_inputs(B, Q, T, 1000, seed=61, pad=9)
+    q = [wl.mla_queries(B, Q, 61, layer, DEV) for layer in range(n)]
+    kv = [wl.latent_cache(B, T, 61, layer, DEV) for layer in range(n)]
+    outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV) for _ in range(n)]
+    dsa.sparse_mla_attn_shared(cfg, q, kv, idx, outs, dsa.alloc_workspace(cfg, B, Q, T, n))
+    torch.cuda.synchronize()
+    for layer in range(n):
+        O, _ = oracle.sparse_mla_attn(f64(q[layer]), f64(kv[layer]), idx.cpu().numpy(), SCALE)
+        check_attention(f64(outs[layer]), O)
+
+
 def test_attention_one_hot_and_empty_rows():
     cfg = dsa.default_config(topk=64)
     B, Q, T = 1, 2, 300
@@ -195,8 +211,18 @@ def test_bad_index_is_reported_not_faulted():
 
 # --------------------------------------------------------------------------- a4/a6: group and MTP
 
-def _group_check(w_, B=None, T=None, rows=None):
-    """Runs one group through the ABI and checks sampled rows against the oracle."""
+def _workspace_scores(ws, B, Q, T):
+    """The group's own indexer scores: a group call leaves them, [B, Q, T] fp32,
+    at the start of its workspace (include/dsa.h)."""
+    return ws[: B * Q * T * 4].view(torch.float32).view(B, Q, T)
+
+
+def _group_check(w_, B=None, T=None, rows=None, score_rows=(), repeat=False):
+    """Runs one group through the ABI and checks sampled rows against the oracle:
+    the index set (boundary ties allowed) and every layer's output; for the rows
+    in `score_rows` also the group's own scores element by element.  With
+    `repeat`, a second group call on the same inputs must give bit-identical
+    indices and outputs."""
     cfg = dsa.default_config(topk=w_.topk)
     inp = wl.make_inputs(w_, DEV, B=B, T=T)
     B, Q, T = inp.q_idx.shape[0], inp.q_idx.shape[1], inp.k_idx.shape[1]
@@ -207,12 +233,16 @@ def _group_check(w_, B=None, T=None, rows=None):
     torch.cuda.synchronize()
     rows = rows if rows is not None else [(b, t) for b in range(B) for t in range(Q)]
     g_idx = idx.cpu().numpy()
+    g_scores = {bt: _workspace_scores(ws, B, Q, T)[bt[0], bt[1]].cpu().double().numpy() for bt in score_rows}
     ties = 0
     for (b, t) in rows:
         pos = int(inp.q_pos[b, t])
         S = oracle.indexer_scores_row(f64(inp.q_idx[b, t]), f64(inp.w[b, t]), f64(inp.k_idx[b]), pos)
+        if (b, t) in g_scores:
+            check_scores_row(g_scores[(b, t)], S, pos)
         o_idx = oracle.topk_select_row(S, pos, w_.topk)
         ties += check_topk_row(g_idx[b, t], o_idx, S, pos, w_.topk)
+        del S
         for layer in range(w_.n_layers):
             # attention over the oracle's own index set, gathering only those rows
             valid = o_idx[o_idx >= 0]
@@ -226,6 +256,16 @@ def _group_check(w_, B=None, T=None, rows=None):
                 rows_g = f64(inp.kv[layer][b, torch.from_numpy(gv).to(DEV)])
                 Og, _ = oracle.sparse_mla_attn_row(f64(inp.q[layer][b, t]), rows_g, np.arange(gv.size), SCALE)
                 check_attention(f64(outs[layer][b, t]), Og)
+    assert not (set(score_rows) - set(rows)), "score rows must be among the sampled rows"
+    if repeat:
+        outs2 = [torch.empty_like(o) for o in outs]
+        idx2 = torch.empty_like(idx)
+        dsa.indexshare_group_forward(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, inp.q, inp.kv, outs2, idx2, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(idx, idx2), "the index set differs between two identical group calls"
+        for a, b_ in zip(outs, outs2):
+            assert torch.equal(a, b_), "the outputs differ between two identical group calls"
+    del inp, ws, outs
     return ties
 
 
@@ -251,6 +291,13 @@ def test_group_equals_four_independent_layers():
         # the group launch may split the slots differently: compare within rounding
         d = (single.float() - outs[layer].float()).abs().max().item()
         assert d <= 4e-3, d
+    # the shared-index entry point (one launch over the four layers, the
+    # launch the group makes) gives the group's outputs bit for bit
+    shared = [torch.empty_like(o) for o in outs]
+    dsa.sparse_mla_attn_shared(cfg, inp.q, inp.kv, idx, shared, ws1)
+    torch.cuda.synchronize()
+    for a, b in zip(shared, outs):
+        assert torch.equal(a, b)
     # and the group's index set is the standalone indexer + top-k
     scores = torch.empty(B, Q, T, device=DEV)
     dsa.indexer_scores(cfg, inp.q_idx, inp.w, inp.k_idx, inp.q_pos, scores)
@@ -333,23 +380,43 @@ def test_group_eight_layers_ragged():
 def test_full_verify_q8_sampled():
     """Multi-token verification: 8 query tokens per sequence (the last accepted
     token and 7 drafts) through one indexer pass, 4 layers, 128K context."""
-    _group_check(wl.VERIFY, rows=[(0, 0), (0, 7), (9, 3), (15, 7)])
+    rows = [(0, 0), (0, 7), (3, 1), (6, 4), (9, 3), (12, 5), (15, 2), (15, 7)]
+    _group_check(wl.VERIFY, rows=rows, score_rows=[(0, 0), (9, 3), (15, 7)])
     torch.cuda.empty_cache()
 
 
 def test_full_decode_128k_sampled():
-    _group_check(wl.DECODE_128K, rows=[(0, 0), (17, 0), (31, 0)])
+    rows = [(0, 0), (9, 0), (17, 0), (31, 0)]
+    _group_check(wl.DECODE_128K, rows=rows, score_rows=[(0, 0), (31, 0)])
     torch.cuda.empty_cache()
 
 
-def test_full_decode_1m_sampled():
-    ties = _group_check(wl.DECODE_1M, rows=[(0, 0), (7, 0)])
+def test_full_decode_1m_sampled_and_deterministic():
+    """The headline workload: 4 of the 8 sequences against the oracle (two with
+    every one of their 1M scores compared element by element), and a second
+    group call bit-identical to the first (the fused histogram uses global
+    atomics, whose order must not leak into the result)."""
+    ties = _group_check(wl.DECODE_1M, rows=[(0, 0), (3, 0), (5, 0), (7, 0)], score_rows=[(0, 0), (7, 0)],
+                        repeat=True)
     print("boundary ties at 1M:", ties)
     torch.cuda.empty_cache()
 
 
+# prefill rows: the first and last query groups of four, the rows around the
+# middle of the chunk, and 20 more spread over it (32 of 4096)
+PREFILL_ROWS = sorted(set([0, 1, 2, 3, 2046, 2047, 2048, 2049, 4092, 4093, 4094, 4095]
+                          + [int(x) for x in np.linspace(5, 4090, 20)]))
+PREFILL_SCORE_ROWS = [0, 1, 3, 4, 1023, 1024, 2047, 2048, 2049, 3071, 3072, 4091, 4092, 4093, 4094, 4095]
+
+
 def test_full_prefill_sampled():
-    _group_check(wl.PREFILL, rows=[(0, 0), (0, 1), (0, 2049), (0, 4095)])
+    """Chunked prefill, 32 of the 4096 query rows against the oracle; 16 of
+    them (the first and last query groups, around the middle and quarter
+    points) with every score compared element by element: the four-query
+    persistent indexer over 131072 keys with its unit ranges crossing groups."""
+    assert len(PREFILL_ROWS) >= 32
+    _group_check(wl.PREFILL, rows=[(0, t) for t in sorted(set(PREFILL_ROWS) | set(PREFILL_SCORE_ROWS))],
+                 score_rows=[(0, t) for t in PREFILL_SCORE_ROWS])
     torch.cuda.empty_cache()
 
 
@@ -367,8 +434,10 @@ def test_full_mtp_sampled():
     dsa.mtp_draft_attn(cfg, idx0, inp.q_steps, inp.kv[0], out, ws)
     torch.cuda.synchronize()
     g_idx = idx0.cpu().numpy()
-    for b in (0, 63):
+    for b in (0, 9, 18, 27, 36, 45, 54, 63):
         S = oracle.indexer_scores_row(f64(inp.q_idx[b, 0]), f64(inp.w[b, 0]), f64(inp.k_idx[b]), T - 1)
+        if b in (0, 63):
+            check_scores_row(scores[b, 0].cpu().double().numpy(), S, T - 1)
         o_idx = oracle.topk_select_row(S, T - 1, 2048)
         check_topk_row(g_idx[b, 0], o_idx, S, T - 1, 2048)
         gv = g_idx[b, 0]
@@ -377,3 +446,41 @@ def test_full_mtp_sampled():
             O, _ = oracle.sparse_mla_attn_row(f64(inp.q_steps[s, b]), rows, np.arange(gv.size), SCALE)
             check_attention(f64(out[s, b]), O)
     torch.cuda.empty_cache()
+
+
+def test_per_layer_indexer_variant():
+    """Row a5 on the GPU: without IndexShare every layer runs its own indexer
+    and top-k (four distinct indexers), the composite the benchmark times
+    against the group; checked against oracle.per_layer_indexer_forward."""
+    w_ = wl.TINY
+    cfg = dsa.default_config()
+    inp = wl.make_inputs(w_, DEV, per_layer_indexers=True)
+    B, Q, T = w_.B, w_.Q, w_.T
+    ws = dsa.alloc_workspace(cfg, B, Q, T, 1)
+    scores = torch.empty(B, Q, T, device=DEV)
+    idxs, outs = [], []
+    for layer in range(w_.n_layers):
+        idx = torch.empty(B, Q, 2048, dtype=torch.int32, device=DEV)
+        out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+        dsa.indexer_scores(cfg, inp.idx_q[layer], inp.idx_w[layer], inp.idx_k[layer], inp.q_pos, scores)
+        dsa.topk_select(cfg, scores, inp.q_pos, idx, ws)
+        dsa.sparse_mla_attn(cfg, inp.q[layer], inp.kv[layer], idx, out, None, ws)
+        idxs.append(idx)
+        outs.append(out)
+    torch.cuda.synchronize()
+    pos = inp.q_pos.cpu().numpy()
+    o_idxs, o_outs = oracle.per_layer_indexer_forward(
+        [f64(x) for x in inp.idx_q], [f64(x) for x in inp.idx_w], [f64(x) for x in inp.idx_k], pos,
+        [f64(q) for q in inp.q], [f64(kv) for kv in inp.kv], 2048, SCALE)
+    for layer in range(w_.n_layers):
+        S = oracle.indexer_scores(f64(inp.idx_q[layer]), f64(inp.idx_w[layer]), f64(inp.idx_k[layer]), pos)
+        g = idxs[layer].cpu().numpy()
+        for t in range(Q):
+            check_topk_row(g[0, t], o_idxs[layer][0, t], S[0, t], int(pos[0, t]), 2048)
+        if np.array_equal(g, o_idxs[layer]):
+            ref = o_outs[layer]
+        else:
+            ref, _ = oracle.sparse_mla_attn(f64(inp.q[layer]), f64(inp.kv[layer]), g, SCALE)
+        check_attention(f64(outs[layer]), ref)
+    # four independent indexers: the layers do not all select the same set
+    assert any(not torch.equal(idxs[0], idxs[layer]) for layer in range(1, w_.n_layers))

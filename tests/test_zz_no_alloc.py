@@ -64,6 +64,14 @@ def test_noalloc_matches_workspace_entry_point_twice():
     _compare(B=2, Q=3, T=7000, k=1000, seed=72)
 
 
+def test_noalloc_at_its_row_limit():
+    # 64 rows: the scratch holds one partial per row, so the key range of each
+    # row runs unsplit in one block (the edge of the partial-result limit)
+    _compare(B=64, Q=1, T=9000, k=2048, seed=74)
+    # 64 rows spread over several query tokens per sequence
+    _compare(B=16, Q=4, T=5000, k=2048, seed=75)
+
+
 def test_noalloc_rejects_more_rows_than_its_scratch_holds():
     cfg = dsa.default_config()
     q, kv, idx = _case(65, 1, 300, 2048, seed=73)
