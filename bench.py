@@ -118,8 +118,8 @@ class ClockSampler:
 
     def summary(self, t0: float, t1: float) -> dict:
         """Samples taken between wall times t0 and t1 (time.time()); the
-        nearest sample when none falls inside (windows shorter than 100 ms)."""
-        self.stop()
+        nearest sample when none falls inside (windows shorter than 100 ms).
+        Read after stop(), once every window has been run."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = self.rows
@@ -311,18 +311,22 @@ def input_bytes(inp: wl.Inputs) -> int:
 
 def read_stream_gbs(dev) -> float:
     """A read-only HBM stream, for context beside the copy peak: the best of
-    10 fp32-accumulated sums over 4 GiB of bf16 (torch's reduction), timed
-    with CUDA events."""
-    x = torch.ones(2 ** 31, dtype=torch.bfloat16, device=dev)
+    several of torch's full reductions (an fp32 sum, an fp32 max and an int32
+    max) over the same 4 GiB buffer, each the best of 8, timed with CUDA
+    events."""
+    x = torch.ones(2 ** 30, dtype=torch.float32, device=dev)
+    ops = (lambda: x.sum(), lambda: x.amax(), lambda: x.view(torch.int32).amax())
     torch.cuda.synchronize()
     best = 0.0
-    for _ in range(12):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        x.sum(dtype=torch.float32)
-        e1.record()
-        e1.synchronize()
-        best = max(best, x.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    for op in ops:
+        op()
+        for _ in range(8):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            op()
+            e1.record()
+            e1.synchronize()
+            best = max(best, x.numel() * 4 / (e0.elapsed_time(e1) / 1e3) / 1e9)
     del x
     torch.cuda.empty_cache()
     return best
@@ -361,7 +365,7 @@ def roofline_of(kernel: str, ms: float, nbytes: int, flops: int, hbm_gbs: float,
             "algorithmic_flops": flops, "achieved_tflops": tfs, "peak_source": f"{peak_src} hbm copy"}
 
 
-def run_ours(args, w: wl.Workload, world: int, rank: int, local: int, clocks, headline: bool = True) -> dict | None:
+def run_ours(args, w: wl.Workload, world: int, rank: int, local: int, headline: bool = True) -> dict | None:
     """Measures one workload: the whole step captured in a CUDA graph and
     timed with events (max over ranks), each kernel of the path timed alone,
     the step end to end through the C ABI with host buffers, and (headline
@@ -474,7 +478,7 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int, clocks, he
     status = dsa.get_device_error(stream)
     if status != 0:
         raise RuntimeError(f"device error during timing: {dsa.status_string(status)}")
-    clk = clocks.summary(t_settle, t_wall1) if clocks is not None else None
+    clock_window = (t_settle, t_wall1)   # summarised once the sampler has stopped
 
     # ---- each kernel of the path alone, timed with events on its own stream
     kst = torch.cuda.Stream(device=dev)
@@ -560,7 +564,7 @@ def run_ours(args, w: wl.Workload, world: int, rank: int, local: int, clocks, he
         "e2e": e2e,
         "gpu_launches": (launches_per_step or 0) * args.steps,
         "gpu_launches_per_step": launches_per_step,
-        "clocks": clk,
+        "clocks": clock_window,
         "step_ms_median": statistics.median(step_ms),
     }
     if headline and w.name == wl.DECODE_1M.name and not args.no_variant and not paged and not fp8:
@@ -844,7 +848,7 @@ def main():
     vis = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
     clocks = ClockSampler(vis[local] if local < len(vis) else local)
     args.read_peak_gbs = None if args.no_read_peak else read_stream_gbs(f"cuda:{local}")
-    res = run_ours(args, w, world, rank, local, clocks, headline=True)
+    res = run_ours(args, w, world, rank, local, headline=True)
     extras = not (args.only_headline or args.batch is not None or args.fp8_indexer or args.paged)
     if extras:
         import gc
@@ -856,11 +860,13 @@ def main():
                 continue
             gc.collect()
             torch.cuda.empty_cache()
-            r = run_ours(args, wl.WORKLOADS[name], world, rank, local, clocks, headline=False)
+            r = run_ours(args, wl.WORKLOADS[name], world, rank, local, headline=False)
             res["workloads"][name] = summary_of(r)
             del r
         args.settle = settle
     clocks.stop()
+    for r in [res] + list(res.get("workloads", {}).values()):
+        r["clocks"] = clocks.summary(*r["clocks"])
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -25,12 +25,12 @@ __device__ __forceinline__ void raise_error(unsigned bits) { atomicOr(&g_error_w
 // (kWaitLimitNs unless the host set another limit).  The waits that drain
 // copies and MMAs still in flight before a block exits always use the full
 // kWaitLimitNs, so a short limit never lets a block leave with work pending.
+// The limit lives in constant memory: it only changes between launches, and
+// a constant-cache hit costs a waiting thread next to nothing.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-__device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+__constant__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
 
-__device__ __forceinline__ unsigned long long wait_limit_ns() {
-  return *static_cast<volatile unsigned long long *>(&g_wait_limit_ns);
-}
+__device__ __forceinline__ unsigned long long wait_limit_ns() { return g_wait_limit_ns; }
 
 __device__ __forceinline__ unsigned long long global_timer_ns() {
   unsigned long long t;
@@ -74,17 +74,49 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, suspending the thread for at most `hint_ns` nanoseconds.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this are served by short suspends and a clock check per poll.
+constexpr unsigned long long kShortWaitLimitNs = 1000000ull;  // 1 ms
+
 // Waits for the phase of parity `parity` to complete.  Gives up after
 // wait_limit_ns(), or as soon as *abort is set by another thread of the block;
-// on giving up it records kErrTimeout, sets *abort and returns false.
+// on giving up it records kErrTimeout, sets *abort and returns false.  With
+// the default limit the clock is read every 64 polls; a short limit (set by
+// the host to make stuck dependencies surface sooner) bounds each suspend by
+// the limit itself and reads the clock at every poll.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
+  const unsigned long long limit = wait_limit_ns();
+  if (limit < kShortWaitLimitNs) {
+    const uint32_t hint = static_cast<uint32_t>(limit > 0 ? limit : 1);
+    for (;;) {
+      if (mbar_try_wait_hint(bar, parity, hint)) return true;
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > limit) {
+        raise_error(kErrTimeout);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > wait_limit_ns()) {
+      if (global_timer_ns() - t0 > limit) {
         raise_error(kErrTimeout);
         *abort = 1;
         return false;
