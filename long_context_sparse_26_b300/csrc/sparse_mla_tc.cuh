@@ -9,48 +9,48 @@
 // "GLM-5.2核心技术解析：IndexShare架构与MTP层优化详解"; 64 heads).
 //
 // Block = (layer, split, query row): it walks kKeys-key windows of its slice
-// of the index set.  Per window:
-//   gather  the selected latent rows in 32-row stages, 16-byte cp.async copies
-//           from the producer warps (a warp keeps only so many copies in
-//           flight, so the gather rate grows with the issuing warps; TMA
-//           gather4 copies of 4 x 128 B would be limited by their issue rate
-//           instead), into a ring of nine 64-dim panels x 128 rows x 128 B in
-//           the 128-byte-swizzled layout the tensor cores read; unused slots
-//           are zero-filled.  The ring is panel-major, so consecutive stages
-//           of a window form one contiguous operand;
-//   GEMM 1  S[64 heads, kKeys] = Q . K^T      tcgen05, M = 64, N = kKeys, K = 576
-//           (Q: nine TMA-loaded panels, resident for the whole block).  The
-//           tensor pipe is fed from shared memory, so its rate follows the
-//           operand bytes per MMA; the ring keeps several stages in flight;
-//   softmax one thread per head reads its S row from tensor memory: masked,
-//           scaled (log2 e folded in), exponentiated against a per-head
-//           reference max, row-summed, and written as bf16 P^T rows into
-//           the window's own RoPE panel (dead once GEMM 1 has read it), so
-//           each window has its own P and the softmax of the next window
-//           never waits for this window's GEMM 2;
+// of the index set through a ring of two window slots.  A slot is nine
+// 64-dim panels x 64 rows x 128 B in the 128-byte-swizzled layout the tensor
+// cores read, and it moves in five panel groups: group g < 4 is panels 2g and
+// 2g+1 (dims 128g..128g+127), group 4 the RoPE panel 8.  Per window:
+//   gather  the selected latent rows, group by group, by 16-byte cp.async
+//           copies from the producer warps (unused slots zero-filled); a
+//           group of the next window is gathered as soon as the window two
+//           back has released it, so gathers overlap the tail of GEMM 2;
+//   GEMM 1  S[64 heads, kKeys] = Q . K^T  tcgen05, M = 64, N = kKeys, K = 576
+//           (Q: nine TMA-loaded panels, resident for the whole block),
+//           consumed group by group as the groups land, so the MMAs overlap
+//           the rest of the gather;
+//   softmax two threads per head (one per 32 keys) read the head's S row from
+//           tensor memory: masked, scaled (log2 e folded in), exponentiated
+//           against a per-head reference max, summed, and written as bf16
+//           P^T rows into the window's RoPE panel (dead once GEMM 1 has read
+//           it);
 //   GEMM 2  O^T[512 dims, 64 heads] += V^T . P^T  tcgen05, M = 128 (4 chunks of
-//           128 dims), N = 64, K = kKeys; V^T is read from the gathered
-//           panels 0..7 as an MN-major operand (no transpose pass).
+//           128 dims), N = 64, K = kKeys, from a thread of its own; V^T is read
+//           from the gathered panels as an MN-major operand (no transpose
+//           pass); chunk c releases group c of the slot as it completes, the
+//           last chunk also group 4 (which held P).
 // The reference max only moves when a head's tile max exceeds it by more than
 // 2^8 (log2 units); then the block rescales that head's O^T column and its
-// running sum.  Anything in between stays within fp32 range, and the final
-// O / l is the same for every choice of reference.
+// running sum before that window's GEMM 2.  Anything in between stays within
+// fp32 range, and the final O / l is the same for every choice of reference.
 //
-// Warp roles (kThreads threads, one block per SM; more than 8 warps puts three
-// on some scheduler, which caps a thread at 168 registers):
-//   producers  rows w, w + kProducerWarps, ... of each stage; warp 0 also
-//              loads the query panels by TMA;
-//   next warp  tensor-memory allocation and GEMM 1 issue (one thread);
-//   last 4     softmax, O^T rescale, epilogue; the first of them also issues
-//              GEMM 2 (one thread), so that GEMM 1 of the next window and
-//              GEMM 2 of this one are issued side by side (one thread issues
-//              these small MMAs at ~54 cycles each, two reach the ~32-48
-//              cycles their shared-memory operands take); warp w owns TMEM lanes
+// Warp roles (kThreads threads, one block per SM):
+//   producers  5 warps: rows w, w + 5, ... of every window; warp 0 also loads
+//              the query panels by TMA;
+//   GEMM 1     two warps, one issuing thread each, on alternate panel groups
+//              into two partial S tiles (the first also allocates tensor
+//              memory); GEMM 2 a third: one thread issues these small MMAs at
+//              about half the rate the tensor pipe takes them, two or three
+//              keep it fed;
+//   last 4     softmax, O^T rescale, epilogue; warp w owns TMEM lanes
 //              32*(w%4)..+31: heads 16*(w%4)..+15 of S (an M = 64 result
-//              sits in lanes 0-15 of each 32-lane quarter) and dims
-//              128c + 32*(w%4)..+31 of O^T chunk c.
-// Tensor memory: O^T in columns 0-255 (chunk c at 64c), S in two buffers of
-// kKeys columns from 256.
+//              sits in lanes 0-15 of each 32-lane quarter; both half-warps
+//              read them, 32 columns each) and dims 128c + 32*(w%4)..+31 of
+//              O^T chunk c.
+// Tensor memory: O^T in columns 0-255 (chunk c at 64c); the two S partials in
+// two window buffers of kKeys columns each, from 256 and from 384.
 // The epilogue stages the block's result in the (then idle) gather buffers
 // and writes it with coalesced 16-byte stores: bf16 and normalised with one
 // split, else the unnormalised fp32 partial plus (reference max, sum) per
@@ -69,28 +69,38 @@ using attn::Params;
 constexpr int kH = 64;
 constexpr int kDv = 512;
 constexpr int kKeys = 64;                            // keys per window (GEMM 1 N, GEMM 2 K)
-constexpr int kStageRows = 32;                       // rows per gather stage
-constexpr int kStages = 4;                           // gather stages in the ring
-constexpr int kWinStages = kKeys / kStageRows;       // gather stages per window
-constexpr int kWindows = kStages / kWinStages;       // windows in the ring
-constexpr int kHalves = kKeys / 32;                  // 32-column TMEM loads per S row
-constexpr int kRingRows = kStages * kStageRows;      // 128
+constexpr int kWindows = 2;                          // window slots in the ring
+constexpr int kRingRows = kWindows * kKeys;          // 128
 constexpr int kPanels = 9;                           // 576 dims / 64
+constexpr int kGroups = 5;                           // panel groups of a window slot
 constexpr int kPanelBytes = kRingRows * 128;         // one 64-dim panel of the ring: 16 KB
 constexpr int kRingBytes = kPanels * kPanelBytes;    // 147456
 constexpr int kQBytes = kPanels * kH * 128;          // 73728
-constexpr int kProducerWarps = 7;
-constexpr int kMmaWarp = kProducerWarps;
-constexpr int kSoftmaxWarp0 = kProducerWarps + 1;
-constexpr int kThreads = 32 * (kProducerWarps + 1 + 4);
+constexpr int kProducerWarps = 5;
+constexpr int kMmaWarp = kProducerWarps;             // tensor-memory allocation, GEMM 1 on groups 0, 2, 4
+constexpr int kMma1bWarp = kProducerWarps + 1;       // GEMM 1 on groups 1, 3
+constexpr int kGemm2Warp = kProducerWarps + 2;       // GEMM 2 issue
+constexpr int kSoftmaxWarp0 = kProducerWarps + 3;    // four softmax warps, one per TMEM lane quarter
+constexpr int kThreads = 32 * (kProducerWarps + 3 + 4);
+constexpr int kRowsPerWarp = (kKeys + kProducerWarps - 1) / kProducerWarps;  // rows of a window per producer warp
+constexpr int kPatA = (kRowsPerWarp + 1) / 2;        // copy instructions of a two-panel group (two rows each)
+constexpr int kPatB = (kRowsPerWarp + 3) / 4;        // copy instructions of the RoPE panel (four rows each)
+// FP8 latent rows are gathered and converted in stages of 32 rows, two per window
+constexpr int kStageRows = 32;
+constexpr int kStages = kRingRows / kStageRows;      // 4
+constexpr int kWinStages = kKeys / kStageRows;       // 2
+constexpr int kHalves = kKeys / 32;                  // 32-column TMEM loads per S row
 constexpr int kTmemCols = 512;
 constexpr int kOCol = 0;
-constexpr int kSCol = 256;
+constexpr int kSCol = 256;                           // S partial of groups 0, 2, 4; two window buffers
+constexpr int kSColB = 384;                          // S partial of groups 1, 3; two window buffers
 constexpr int kSmallBytes = 1024;
 constexpr int kSmemBytes = 1024 + kQBytes + kRingBytes + kSmallBytes;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
+static_assert(kSoftmaxWarp0 % 4 == 0, "softmax warp w reads TMEM lane quarter w % 4");
 static_assert(kRingBytes >= kH * kDv * 4, "the epilogue stages an fp32 partial in the gather ring");
-static_assert(kKeys % kStageRows == 0 && kStages % kWinStages == 0 && kKeys % 32 == 0, "windows tile the ring");
+static_assert(kKeys % kStageRows == 0 && kKeys % 32 == 0 && kKeys == 64, "windows of 64 keys");
+static_assert(kSColB + 2 * kKeys <= kTmemCols && kSCol + 2 * kKeys <= kSColB, "S partials fit the allocation");
 constexpr float kRescaleLog2 = 8.0f;                 // rescale when the max grows by > 2^8
 
 struct Maps {
@@ -128,6 +138,29 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 2^x by the MUFU approximation (ex2.approx.ftz.f32: 2^-inf = +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Lanes 0-15 of the warp's quarter, twice: threads 0-15 get lane t, columns
+// [taddr, taddr + 32); threads 16-31 get lane t - 16, columns [taddr + 32,
+// taddr + 64) (16x32bx2 shape, half-split offset 32 columns).  Not waited.
+__device__ __forceinline__ void tmem_ld_16x32bx2_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32], 32;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
 
 // 32 lanes x 8 columns, load (waited) and store.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
@@ -178,19 +211,21 @@ __device__ __forceinline__ int checked_pos(int raw, int T, bool report) {
 
 struct Small {
   alignas(16) float xa[2][kH];    // per-head rescale factors (1/l for the epilogue)
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kWindows][kGroups];   // a group of a window slot has landed (producer arrivals)
+  uint64_t empty[kWindows][kGroups];  // a group of a window slot is free (GEMM 2 commits)
   uint64_t s_full[2];
   uint64_t s_empty[2];
-  uint64_t p_full;
-  uint64_t p_free;
+  uint64_t p_full;                // every softmax warp has written its P rows and its flags
+  uint64_t p_free;                // GEMM 2 of the window has completed
+  uint64_t resc_done;             // every softmax warp has rescaled its O^T lanes
   uint64_t q_full;
   uint64_t mma_done;
+  uint64_t mma1b_done;
   uint64_t mma2_done;
   uint64_t staged[kProducerWarps][kStages];  // FP8 latent rows: a warp's copies of a stage have landed
   uint32_t tmem_slot;
   int abort;
-  int status[2][4];               // per softmax warp, per iteration parity: 1 = ok
+  int status[2][4];               // per softmax warp, per window parity: 1 = ok
   int need[2][4];                 // per softmax warp: a head of it moves its reference max
 };
 static_assert(sizeof(Small) <= kSmallBytes, "small shared region");
@@ -239,20 +274,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t *irow = p.idx + (size_t)row * p.K;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sm->full[i], 32 * kProducerWarps);
-      mbar_init(&sm->empty[i], 1);
+    for (int w = 0; w < kWindows; ++w)
+      for (int g = 0; g < kGroups; ++g) {
+        mbar_init(&sm->full[w][g], 32 * kProducerWarps);
+        mbar_init(&sm->empty[w][g], 1);
+      }
+    for (int i = 0; i < kStages; ++i)
       for (int w = 0; w < kProducerWarps; ++w) mbar_init(&sm->staged[w][i], 32);
-    }
-    // (a window j uses stages 2*(j%2) and 2*(j%2)+1)
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm->s_full[i], 1);
+      mbar_init(&sm->s_full[i], 2);  // both GEMM 1 issuers commit
       mbar_init(&sm->s_empty[i], 4);
     }
     mbar_init(&sm->p_full, 4);
     mbar_init(&sm->p_free, 1);
+    mbar_init(&sm->resc_done, 4);
     mbar_init(&sm->q_full, 1);
     mbar_init(&sm->mma_done, 1);
+    mbar_init(&sm->mma1b_done, 1);
     mbar_init(&sm->mma2_done, 1);
     sm->abort = 0;
     fence_mbar_init();
@@ -279,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr size_t kRowBytes = F8KV ? attn::kF8RowBytes : (kDv + 64) * 2;
     const uint8_t *kvb = reinterpret_cast<const uint8_t *>(p.kv[layer]) + (paged ? 0 : (size_t)b * p.T * kRowBytes);
     // row of kvb holding position pos (-1: none); the block-table load is
-    // issued a stage before the row is used
+    // issued a window before the row is used
     auto row_of = [&](int pos) -> int {
       if (pos < 0 || !paged) return pos;
       const int page = pos / p.page_size;
@@ -290,57 +328,110 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return phys * p.page_size + (pos - page * p.page_size);
     };
-    // gather stage g (g = 0, 1, ...) holds index slots 32g..32g+31 of this block
-    // in ring stage g % 4; lane l holds slot l of stage g, loaded three stages ahead
-    const int nstage = nblk * kWinStages;
-    auto load_slot = [&](int g) -> int { return g < nstage ? slot_raw(irow, slot0 + g * kStageRows + lane, p.K) : -1; };
+    const uint32_t k0 = smem_u32(sK);
     if constexpr (!F8KV) {
-      int n1 = load_slot(0), n2 = load_slot(1), n3 = load_slot(2);
-      int next_row = row_of(checked_pos(n1, p.T, warp == 0));
-      for (int g = 0; g < nstage; ++g) {
-        const int cur = next_row;
-        n1 = n2;
-        n2 = n3;
-        n3 = load_slot(g + 3);
-        next_row = row_of(checked_pos(n1, p.T, warp == 0));
-        const int s = g % kStages;
-        const uint32_t ph = static_cast<uint32_t>(g / kStages) & 1u;
-        if (!warp_wait(&sm->empty[s], ph ^ 1u, abort_flag)) break;
-        const uint32_t sbase = smem_u32(sK) + s * kStageRows * 128;
-        for (int r = warp; r < kStageRows; r += kProducerWarps) {
-          const int pos = __shfl_sync(0xffffffffu, cur, r);
-          const uint8_t *src = kvb + (size_t)(pos < 0 ? 0 : pos) * kRowBytes;
-          const uint32_t nbytes = pos < 0 ? 0u : 16u;  // unused slot: zero-filled row
-          const uint32_t rbase = sbase + r * 128;       // ring row s*32 + r; (s*32 + r) % 8 == r % 8
+      // lane l holds index slots l and l + 32 of a window: the raw slots two
+      // windows ahead, their cache rows one window ahead
+      auto slot_of = [&](int jj, int half) -> int {
+        return jj < nblk ? slot_raw(irow, slot0 + jj * kKeys + half * 32 + lane, p.K) : -1;
+      };
+      int raw1_lo = slot_of(1, 0), raw1_hi = slot_of(1, 1);
+      int raw2_lo = slot_of(2, 0), raw2_hi = slot_of(2, 1);
+      int nxt_lo = row_of(checked_pos(slot_of(0, 0), p.T, warp == 0));
+      int nxt_hi = row_of(checked_pos(slot_of(0, 1), p.T, warp == 0));
+      bool stop = false;
+      for (int jj = 0; jj < nblk && !stop; ++jj) {
+        const int cur_lo = nxt_lo, cur_hi = nxt_hi;
+        nxt_lo = row_of(checked_pos(raw1_lo, p.T, warp == 0));
+        nxt_hi = row_of(checked_pos(raw1_hi, p.T, warp == 0));
+        raw1_lo = raw2_lo;
+        raw1_hi = raw2_hi;
+        raw2_lo = slot_of(jj + 3, 0);
+        raw2_hi = slot_of(jj + 3, 1);
+        const int w = jj % kWindows;
+        const uint32_t ph = static_cast<uint32_t>(jj / kWindows) & 1u;
+        // this warp owns window rows warp + 5k.  Copy pattern A (a two-panel
+        // group, 16 chunks a row) covers two rows an instruction, lane l
+        // taking row k = 2i + l/16; pattern B (the RoPE panel, 8 chunks a
+        // row) four rows, k = 4i + l/8.  Per lane: the cache row of each
+        // instruction and its ring row (-1: no such row in the window)
+        int posA[kPatA], ringA[kPatA], posB[kPatB], ringB[kPatB];
 #pragma unroll
-          for (int cc = 0; cc < 3; ++cc) {
-            const int c = lane + 32 * cc;  // 16-byte chunk of the 1152-byte row
-            if (c < 72) cp_async_16(rbase + (c >> 3) * kPanelBytes + (((c & 7) ^ (r & 7)) << 4), src + c * 16, nbytes);
-          }
+        for (int i = 0; i < kPatA; ++i) {
+          const int k = 2 * i + (lane >> 4);
+          const int r = warp + kProducerWarps * k;
+          const int vlo = __shfl_sync(0xffffffffu, cur_lo, r & 31);
+          const int vhi = __shfl_sync(0xffffffffu, cur_hi, r & 31);
+          posA[i] = r < 32 ? vlo : vhi;
+          ringA[i] = (k < kRowsPerWarp && r < kKeys) ? w * kKeys + r : -1;
         }
-        cp_async_mbar_arrive(&sm->full[s]);
+#pragma unroll
+        for (int i = 0; i < kPatB; ++i) {
+          const int k = 4 * i + (lane >> 3);
+          const int r = warp + kProducerWarps * k;
+          const int vlo = __shfl_sync(0xffffffffu, cur_lo, r & 31);
+          const int vhi = __shfl_sync(0xffffffffu, cur_hi, r & 31);
+          posB[i] = r < 32 ? vlo : vhi;
+          ringB[i] = (k < kRowsPerWarp && r < kKeys) ? w * kKeys + r : -1;
+        }
+        for (int gi = 0; gi < kGroups; ++gi) {
+          if (!warp_wait(&sm->empty[w][gi], ph ^ 1u, abort_flag)) {
+            stop = true;
+            break;
+          }
+          if (gi < kGroups - 1) {
+            // panels 2gi and 2gi + 1: bytes 256 gi .. 256 gi + 255 of the row
+            const int c = lane & 15;
+            const uint32_t pbase = k0 + (2 * gi + (c >> 3)) * kPanelBytes;
+#pragma unroll
+            for (int i = 0; i < kPatA; ++i) {
+              if (ringA[i] >= 0) {
+                const int pos = posA[i];
+                const uint8_t *src = kvb + (size_t)(pos < 0 ? 0 : pos) * kRowBytes + gi * 256 + c * 16;
+                cp_async_16(pbase + ringA[i] * 128 + (((c & 7) ^ (ringA[i] & 7)) << 4), src, pos < 0 ? 0u : 16u);
+              }
+            }
+          } else {
+            // panel 8 (RoPE): bytes 1024 .. 1151 of the row
+            const int c = lane & 7;
+            const uint32_t pbase = k0 + 8 * kPanelBytes;
+#pragma unroll
+            for (int i = 0; i < kPatB; ++i) {
+              if (ringB[i] >= 0) {
+                const int pos = posB[i];
+                const uint8_t *src = kvb + (size_t)(pos < 0 ? 0 : pos) * kRowBytes + 1024 + c * 16;
+                cp_async_16(pbase + ringB[i] * 128 + ((c ^ (ringB[i] & 7)) << 4), src, pos < 0 ? 0u : 16u);
+              }
+            }
+          }
+          cp_async_mbar_arrive(&sm->full[w][gi]);
+        }
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
     } else {
-      // FP8 latent rows, dequantised in shared memory.  A warp owns rows
-      // warp, warp + 7, ... of every stage.  Each 656-byte row first lands by
-      // cp.async in its own ring lines (41 16-byte chunks: chunk c in panel
-      // c / 8, slot c % 8, unswizzled), tracked by the warp's own mbarrier
-      // per stage; then the warp reads its rows back, syncs, and writes the
-      // bf16 row over the same lines in the swizzled operand layout.  Only
-      // the owning warp touches a row's lines, so a warp sync orders the
-      // reads before the writes.  The warp interleaves issuing copies (as
-      // ring stages free up) with converting stages whose copies landed, so
-      // several stages stay in flight.
+      // FP8 latent rows, dequantised in shared memory, in stages of 32 rows
+      // (stage i holds index slots 32i..32i+31 in ring rows 32 (i % 4) ..:
+      // window i / 2 in slot (i / 2) % 2).  A warp owns rows warp, warp + 5,
+      // ... of every stage.  Each 656-byte row first lands by cp.async in its
+      // own ring lines (41 16-byte chunks: chunk c in panel c / 8, slot c % 8,
+      // unswizzled), tracked by the warp's own mbarrier per stage; then the
+      // warp reads its rows back, syncs, and writes the bf16 row over the same
+      // lines in the swizzled operand layout.  Only the owning warp touches a
+      // row's lines, so a warp sync orders the reads before the writes.  The
+      // warp interleaves issuing copies (once every group of the window's
+      // slot is free) with converting stages whose copies landed, so several
+      // stages stay in flight; a window's groups are released to GEMM 1 once
+      // both of its stages are converted.
       constexpr int kRPW = (kStageRows + kProducerWarps - 1) / kProducerWarps;  // rows per warp and stage
-      const uint32_t k0s = smem_u32(sK);
+      const int nstage = nblk * kWinStages;
+      auto load_slot = [&](int g) -> int { return g < nstage ? slot_raw(irow, slot0 + g * kStageRows + lane, p.K) : -1; };
       // rows of stage i (per lane: slot i*32 + lane), slot loads one issue ahead
       int raw_cur = load_slot(0), raw_next = load_slot(1);
       auto issue = [&](int i) {
         const int rows_i = row_of(checked_pos(raw_cur, p.T, warp == 0));
         raw_cur = raw_next;
         raw_next = load_slot(i + 2);
-        const uint32_t sbase = k0s + (i % kStages) * kStageRows * 128;
+        const uint32_t sbase = k0 + (i % kStages) * kStageRows * 128;
 #pragma unroll
         for (int j = 0; j < kRPW; ++j) {
           const int r = warp + kProducerWarps * j;
@@ -359,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cp_async_mbar_arrive(&sm->staged[warp][i % kStages]);
       };
       auto convert = [&](int i) {
-        const uint32_t sbase = k0s + (i % kStages) * kStageRows * 128;
+        const uint32_t sbase = k0 + (i % kStages) * kStageRows * 128;
         uint4 code[kRPW], rope[kRPW];
         float scale[kRPW];
 #pragma unroll
@@ -403,16 +494,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&sm->full[i % kStages]);
+        if (i % kWinStages == kWinStages - 1)
+          for (int g = 0; g < kGroups; ++g) mbar_arrive(&sm->full[(i / kWinStages) % kWindows][g]);
       };
       int issued = 0, conv = 0;
       unsigned long long t_idle = 0;
       while (conv < nstage) {
         bool prog = false;
         if (issued < nstage) {
-          const uint32_t ph = static_cast<uint32_t>(issued / kStages) & 1u;
-          int ok = lane == 0 ? (mbar_try_wait(&sm->empty[issued % kStages], ph ^ 1u) ? 1 : 0) : 0;
-          if (__shfl_sync(0xffffffffu, ok, 0)) {
+          int ok = 1;
+          if (issued % kWinStages == 0) {
+            // the first stage of a window waits for every group of its slot
+            const int wv = issued / kWinStages;
+            const uint32_t ph = static_cast<uint32_t>(wv / kWindows) & 1u;
+            if (lane == 0)
+              for (int g = 0; g < kGroups; ++g) ok &= mbar_try_wait(&sm->empty[wv % kWindows][g], ph ^ 1u) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+          }
+          if (ok) {
             issue(issued);
             ++issued;
             prog = true;
@@ -449,48 +548,107 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("cp.async.wait_all;" ::: "memory");
     }
     if (q_issued && lane == 0) mbar_wait_drain(&sm->q_full, 0, kWaitLimitNs);
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kMmaWarp || warp == kMma1bWarp) {
+    // ------------------------------------------------------------ GEMM 1 issuers
+    // Two threads share GEMM 1 (one thread issues these small MMAs at about
+    // half the rate the tensor pipe takes them): the MMA warp on groups 0, 2
+    // and 4 into the S partial at kSCol, the next warp on groups 1 and 3 into
+    // the one at kSColB; the softmax adds the two.
+    const bool part_a = warp == kMmaWarp;
     if (lane == 0 && nblk > 0) {
       constexpr uint32_t id1 = idesc(64, kKeys, false, false);
       const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK);
       bool ok = mbar_wait_bounded(&sm->q_full, 0, abort_flag);
-      // GEMM 1 of each window in order, once its rows have landed and its S
-      // buffer is free; GEMM 2 is issued by the first softmax warp, so the two
-      // GEMMs of neighbouring windows are issued side by side (one issuing
-      // thread cannot keep the tensor pipe fed with these small MMAs)
+      // GEMM 1 of each window in order, once its S buffer is free, group by
+      // group as the groups land
       for (int g1 = 0; ok && g1 < nblk; ++g1) {
         const int w = g1 % kWindows;  // window slot in the ring
         const int sb = g1 & 1;        // S buffer
         const uint32_t ph = static_cast<uint32_t>(g1 / kWindows) & 1u;
         ok = mbar_wait_bounded(&sm->s_empty[sb], (static_cast<uint32_t>(g1 >> 1) & 1u) ^ 1u, abort_flag);
-        for (int h = 0; h < kWinStages && ok; ++h) ok = mbar_wait_bounded(&sm->full[w * kWinStages + h], ph, abort_flag);
-        if (!ok) break;
-        fence_proxy_async_smem();  // the gathered rows were written through the generic proxy
-        tc_fence_after();
-        const uint32_t d = tmem_base + kSCol + sb * kKeys;
+        const uint32_t d = tmem_base + (part_a ? kSCol : kSColB) + sb * kKeys;
         const uint32_t ks = k0 + w * kKeys * 128;  // the window's rows in every panel
+        bool first = true;
+        for (int gi = part_a ? 0 : 1; ok && gi < kGroups; gi += 2) {
+          ok = mbar_wait_bounded(&sm->full[w][gi], ph, abort_flag);
+          if (!ok) break;
+          fence_proxy_async_smem();  // the gathered rows were written through the generic proxy
+          tc_fence_after();
+          const int np = gi < kGroups - 1 ? 2 : 1;
+          for (int pi = 0; pi < np; ++pi) {
+            const int pp = gi < kGroups - 1 ? 2 * gi + pi : 8;
 #pragma unroll
-        for (int kk = 0; kk < kPanels * 4; ++kk) {
-          const uint32_t qoff = (kk >> 2) * (kH * 128) + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-          tc_mma_bf16(d, desc_sw128(q0 + qoff, 16, 1024), desc_sw128(ks + koff, 16, 1024), id1, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t qoff = pp * (kH * 128) + kk * 32;
+              const uint32_t koff = pp * kPanelBytes + kk * 32;
+              tc_mma_bf16(d, desc_sw128(q0 + qoff, 16, 1024), desc_sw128(ks + koff, 16, 1024), id1,
+                          first ? 0u : 1u);
+              first = false;
+            }
+          }
         }
+        if (!ok) break;
         tc_commit(&sm->s_full[sb]);
       }
-      tc_commit(&sm->mma_done);
-      mbar_wait_drain(&sm->mma_done, 0, kWaitLimitNs);
+      uint64_t *done = part_a ? &sm->mma_done : &sm->mma1b_done;
+      tc_commit(done);
+      mbar_wait_drain(done, 0, kWaitLimitNs);
+    }
+  } else if (warp == kGemm2Warp) {
+    // ------------------------------------------------------------ GEMM 2 issuer
+    // GEMM 2 of window j once every softmax warp has written its P rows (and,
+    // when a head's reference max moved, rescaled its O^T lanes):
+    // O^T[512 dims, 64 heads] += V^T . P^T, chunk by chunk, each chunk's
+    // commit releasing the panel group it read; the last also releases the
+    // RoPE panel that held P
+    if (lane == 0 && nblk > 0) {
+      constexpr uint32_t id2 = idesc(128, 64, true, false);
+      int issued = 0;
+      uint32_t nresc = 0;
+      for (int j = 0; j < nblk; ++j) {
+        if (!mbar_wait_bounded(&sm->p_full, static_cast<uint32_t>(j) & 1u, abort_flag)) break;
+        const volatile int *nd = sm->need[j & 1];
+        const bool any = (nd[0] | nd[1] | nd[2] | nd[3]) != 0;
+        if (any && j > 0) {
+          if (!mbar_wait_bounded(&sm->resc_done, nresc & 1u, abort_flag)) break;
+          ++nresc;
+        }
+        tc_fence_after();
+        const int w = j % kWindows;
+        const uint32_t ks = smem_u32(sK) + w * kKeys * 128;
+        const uint32_t p0 = smem_u32(sK) + 8 * kPanelBytes + w * kKeys * 128;  // P^T
+#pragma unroll
+        for (int c = 0; c < kDv / 128; ++c) {
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            const uint64_t ad = desc_sw128(ks + 2 * c * kPanelBytes + kk * 16 * 128, kPanelBytes, 1024);
+            const uint64_t bd = desc_sw128(p0 + kk * 32, 16, 1024);
+            tc_mma_bf16(tmem_base + kOCol + c * 64, ad, bd, id2, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&sm->empty[w][c]);
+        }
+        tc_commit(&sm->empty[w][kGroups - 1]);
+        tc_commit(&sm->p_free);
+        ++issued;
+      }
+      // every GEMM 2 issued is complete before tensor memory is freed
+      if (issued > 0) {
+        tc_commit(&sm->mma2_done);
+        mbar_wait_drain(&sm->mma2_done, 0, kWaitLimitNs);
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int q4 = warp & 3;                         // TMEM lane quarter of this warp
     const int w4 = warp - kSoftmaxWarp0;             // index among the softmax warps
-    const int head = q4 * 16 + lane;                 // meaningful for lane < 16
-    const bool owner = lane < 16;
+    // the two half-warps share the 16 heads of the quarter: lane l takes head
+    // 16 q4 + l % 16 and keys 32 (l / 16) .. +31 of every window
+    const int hh = lane >> 4;
+    const int head = q4 * 16 + (lane & 15);
+    const bool owner = lane < 16;                    // writes the head's per-head results
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
     float m_ref = -INFINITY, l = 0.0f;
     bool all_ok = true;
-    bool gemm2_issued = false;  // first softmax warp, lane 0: GEMM 2 issued
     bool late_fail = false;     // a wait failed after this window's status exchange
     // validity of window j's keys (bit k of word h = key 32h + k), from the
     // index set itself; slots are loaded two windows ahead, checked when used
@@ -513,133 +671,103 @@ __global__ void __launch_bounds__(kThreads, 1)
         n2[h] = load_slot(j + 2, h);
       }
       bool ok = warp_wait(&sm->s_full[sb], static_cast<uint32_t>(j >> 1) & 1u, abort_flag);
-      uint32_t sv[kKeys];  // raw scores, then (in place) scaled and masked logits
+      uint32_t sv[32];  // this lane's 32 raw scores (the two partials added), then scaled, masked logits
       float mt = -INFINITY;
       if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int h = 0; h < kHalves; ++h)
-          tmem_ld_32x32b_x32_nowait(tmem_base + lane_addr + kSCol + sb * kKeys + 32 * h,
-                                    *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * h));
+        uint32_t t[32];
+        tmem_ld_16x32bx2_x32(tmem_base + lane_addr + kSCol + sb * kKeys, sv);
+        tmem_ld_16x32bx2_x32(tmem_base + lane_addr + kSColB + sb * kKeys, t);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->s_empty[sb]);
+        const uint32_t mk = hh ? mask[1] : mask[0];
 #pragma unroll
-        for (int k = 0; k < kKeys; ++k) {
-          const float v = ((mask[k >> 5] >> (k & 31)) & 1u) ? __uint_as_float(sv[k]) * p.scale_log2 : -INFINITY;
+        for (int k = 0; k < 32; ++k) {
+          const float v = ((mk >> k) & 1u) ? (__uint_as_float(sv[k]) + __uint_as_float(t[k])) * p.scale_log2
+                                           : -INFINITY;
           sv[k] = __float_as_uint(v);
           mt = fmaxf(mt, v);
         }
       }
-      const bool need = ok && owner && mt > m_ref + kRescaleLog2;
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));  // the head's window max (both half-warps)
+      if (late_fail) ok = false;
+      const bool need = ok && mt > m_ref + kRescaleLog2;
       const float m_new = need ? mt : m_ref;
-      const float alpha = need ? exp2f(m_ref - m_new) : 1.0f;
-      // this window's probabilities against the (possibly moved) reference,
-      // packed to bf16 now so the logits are dead before any O^T rescale
-      uint32_t pk[kKeys / 2];
-      float rs = 0.0f;
-      if (ok && owner) {
+      const float alpha = need ? fast_exp2(m_ref - m_new) : 1.0f;
+      float rs = 0.0f;  // this lane's share of the head's window sum
+      if (ok) {
+        // this window's probabilities against the (possibly moved) reference,
+        // as bf16 P^T row `head` in the window's RoPE panel (panel 8 of its
+        // ring slot): GEMM 1 of this window, its only other reader, has
+        // completed, and the panel is not refilled before GEMM 2 of this
+        // window has read it
         const float ref = m_new == -INFINITY ? 0.0f : m_new;
+        uint8_t *prow = sK + 8 * kPanelBytes + (j % kWindows) * kKeys * 128 + head * 128;
 #pragma unroll
-        for (int e = 0; e < kKeys / 2; ++e) {
-          const float a = exp2f(__uint_as_float(sv[2 * e]) - ref);
-          const float bq = exp2f(__uint_as_float(sv[2 * e + 1]) - ref);
-          rs += a + bq;
-          pk[e] = pack_bf16x2(a, bq);
+        for (int cc = 0; cc < 4; ++cc) {
+          const int c = 4 * hh + cc;  // 16-byte chunk of the row: keys 8c .. 8c + 7
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = fast_exp2(__uint_as_float(sv[8 * cc + 2 * e]) - ref);
+            const float bq = fast_exp2(__uint_as_float(sv[8 * cc + 2 * e + 1]) - ref);
+            rs += a + bq;
+            pk[e] = pack_bf16x2(a, bq);
+          }
+          *reinterpret_cast<uint4 *>(prow + ((c ^ (head & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
-      if (late_fail) ok = false;
-      const unsigned any_need = __ballot_sync(0xffffffffu, need);
       if (owner) sm->xa[j & 1][head] = alpha;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      const unsigned any_need = __ballot_sync(0xffffffffu, need);
       if (lane == 0) {
-        sm->status[j & 1][w4] = ok ? 1 : 0;
         sm->need[j & 1][w4] = any_need ? 1 : 0;
+        sm->status[j & 1][w4] = ok ? 1 : 0;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->p_full);
       named_bar_sync(1, 128);
       all_ok = sm->status[j & 1][0] && sm->status[j & 1][1] && sm->status[j & 1][2] && sm->status[j & 1][3];
       if (!all_ok) break;
       const bool rescale = sm->need[j & 1][0] || sm->need[j & 1][1] || sm->need[j & 1][2] || sm->need[j & 1][3];
-      // P needs no wait for the previous window's GEMM 2: each window writes
-      // its own P (below).  Only a rescale of O^T waits for that GEMM 2 (its
-      // phase is the latest one: GEMM 2 of this window is not issued yet).  A
-      // failed wait skips the rescale and fails this warp at the next
-      // window's barrier (or at the epilogue's), where every warp stops.
-      if (rescale && j > 0 && !warp_wait(&sm->p_free, static_cast<uint32_t>(j - 1) & 1u, abort_flag))
-        late_fail = true;
-      if (rescale && j > 0 && !late_fail) {
-        // O^T column h *= alpha[h] on this warp's 32 lanes of every chunk
-        // (rare: 8 columns at a time keeps the registers of the hot path free)
-        tc_fence_after();
+      if (rescale && j > 0) {
+        // O^T column h *= alpha[h] on this warp's 32 lanes of every chunk,
+        // once the previous window's GEMM 2 has completed and before this
+        // window's is issued (rare: 8 columns at a time keeps the registers
+        // of the hot path free).  A failed wait skips the rescale and fails
+        // this warp at the next window's exchange (or at the epilogue's)
+        if (!warp_wait(&sm->p_free, static_cast<uint32_t>(j - 1) & 1u, abort_flag)) {
+          late_fail = true;
+        } else {
+          tc_fence_after();
 #pragma unroll 1
-        for (int g = 0; g < (kDv / 128) * (kH / 8); ++g) {
-          const int c = g / (kH / 8), h0 = (g % (kH / 8)) * 8;
-          const uint32_t taddr = tmem_base + lane_addr + kOCol + c * 64 + h0;
-          uint32_t r[8];
-          tmem_ld8(taddr, r);
+          for (int g = 0; g < (kDv / 128) * (kH / 8); ++g) {
+            const int c = g / (kH / 8), h0 = (g % (kH / 8)) * 8;
+            const uint32_t taddr = tmem_base + lane_addr + kOCol + c * 64 + h0;
+            uint32_t r[8];
+            tmem_ld8(taddr, r);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * sm->xa[j & 1][h0 + i]);
-          tmem_st8(taddr, r);
+            for (int i = 0; i < 8; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * sm->xa[j & 1][h0 + i]);
+            tmem_st8(taddr, r);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->resc_done);
       }
       if (need) {
         m_ref = m_new;
         l *= alpha;
       }
-      if (owner) {
-        // P^T row `head` goes to the window's own RoPE panel (panel 8 of its
-        // ring slot): GEMM 1 of this window, its only reader, has completed,
-        // and the slot is not refilled before GEMM 2 of this window has read it
-        uint8_t *prow = sK + 8 * kPanelBytes + (j % kWindows) * kKeys * 128 + head * 128;
-#pragma unroll
-        for (int c = 0; c < kKeys / 8; ++c)
-          *reinterpret_cast<uint4 *>(prow + ((c ^ (head & 7)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        l += rs;
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->p_full);
-      if (w4 == 0) {
-        // GEMM 2 of window j once every softmax warp has written its P rows:
-        // O^T[512 dims, 64 heads] += V^T . P^T, then the window's stages
-        // (which hold its P) are released as these MMAs complete
-        int issued = 1;
-        if (lane == 0) {
-          issued = mbar_wait_bounded(&sm->p_full, static_cast<uint32_t>(j) & 1u, abort_flag) ? 1 : 0;
-          if (issued) {
-            tc_fence_after();
-            constexpr uint32_t id2 = idesc(128, 64, true, false);
-            const uint32_t ks = smem_u32(sK) + (j % kWindows) * kKeys * 128;
-            const uint32_t p0 = smem_u32(sK) + 8 * kPanelBytes + (j % kWindows) * kKeys * 128;  // P^T
-#pragma unroll
-            for (int c = 0; c < kDv / 128; ++c) {
-#pragma unroll
-              for (int kk = 0; kk < kKeys / 16; ++kk) {
-                const uint64_t ad = desc_sw128(ks + 2 * c * kPanelBytes + kk * 16 * 128, kPanelBytes, 1024);
-                const uint64_t bd = desc_sw128(p0 + kk * 32, 16, 1024);
-                tc_mma_bf16(tmem_base + kOCol + c * 64, ad, bd, id2, (j > 0 || kk > 0) ? 1u : 0u);
-              }
-            }
-            for (int h = 0; h < kWinStages; ++h) tc_commit(&sm->empty[(j % kWindows) * kWinStages + h]);
-            tc_commit(&sm->p_free);
-            gemm2_issued = true;
-          }
-        }
-        // a failed wait fails this warp's status at the next window's barrier
-        if (!__shfl_sync(0xffffffffu, issued, 0)) late_fail = true;
-      }
-    }
-    if (gemm2_issued) {
-      // every GEMM 2 this thread issued is complete before tensor memory is
-      // freed, whatever path the loop took
-      tc_commit(&sm->mma2_done);
-      mbar_wait_drain(&sm->mma2_done, 0, kWaitLimitNs);
+      l += rs;
     }
 
     // ---- epilogue: O^T / l per head, staged in the idle gather buffers
+    l += __shfl_xor_sync(0xffffffffu, l, 16);  // the head's sum: both half-warps' shares
     bool ok = all_ok && !late_fail;
     if (nblk > 0 && ok) ok = warp_wait(&sm->p_free, static_cast<uint32_t>(nblk - 1) & 1u, abort_flag);
     float *inv_l = sm->xa[0];
