@@ -273,6 +273,47 @@ dsa_status_t dsa_indexshare_group_forward_fp8kv(const dsa_config_t *cfg, const u
                                                 dsa_bf16_t *const *out, int32_t *idx_out, void *ws, size_t ws_bytes,
                                                 dsa_stream_t stream);
 
+/* FP8 caches in the paged layout (the pages' serving stack runs the FP8 KV
+ * cache and PagedAttention together: "GLM-5.2 Explained: 1M Token Context AI
+ * Agent Model", §5, Deployment Reference).  Every pool shares the one block
+ * table of `pages` (the dsa_pages_t rules above):
+ *   k8_pool      [num_pages, page_size, 128] u8   E4M3 indexer key codes
+ *   k_scale_pool [num_pages, page_size]      fp32 their row scales
+ *   kv8_pool(s)  [num_pages, page_size, 656] u8   FP8 latent rows (format above)
+ *   kv_pools     [num_pages, page_size, 576] bf16 bf16 latent rows
+ * Position s of sequence b reads row s % page_size of page
+ * block_table[b * max_pages + s / page_size] in every pool; a page outside
+ * [0, num_pages) is reported (DSA_ERR_DEVICE_CHECK) and reads page 0.
+ * Results equal the contiguous FP8 entry points' on the caches the pools
+ * stand for, bit for bit. */
+dsa_status_t dsa_indexer_scores_fp8_paged(const dsa_config_t *cfg, const uint8_t *q_idx8, const float *q_scale,
+                                          const float *w, const uint8_t *k8_pool, const float *k_scale_pool,
+                                          const dsa_pages_t *pages, const int32_t *q_pos, int B, int Q, int T,
+                                          float *scores, dsa_stream_t stream);
+
+dsa_status_t dsa_sparse_mla_attn_fp8_paged(const dsa_config_t *cfg, const dsa_bf16_t *q, const uint8_t *kv8_pool,
+                                           const dsa_pages_t *pages, const int32_t *idx, int B, int Q, int T,
+                                           dsa_bf16_t *out, float *lse, void *ws, size_t ws_bytes,
+                                           dsa_stream_t stream);
+
+/* FP8 indexer caches, bf16 latent pools. */
+dsa_status_t dsa_indexshare_group_forward_fp8_paged(const dsa_config_t *cfg, const uint8_t *q_idx8,
+                                                    const float *q_scale, const float *w, const uint8_t *k8_pool,
+                                                    const float *k_scale_pool, const int32_t *q_pos,
+                                                    const dsa_bf16_t *const *q, const dsa_bf16_t *const *kv_pools,
+                                                    int n_layers, const dsa_pages_t *pages, int B, int Q, int T,
+                                                    dsa_bf16_t *const *out, int32_t *idx_out, void *ws,
+                                                    size_t ws_bytes, dsa_stream_t stream);
+
+/* FP8 indexer caches and FP8 latent pools. */
+dsa_status_t dsa_indexshare_group_forward_fp8kv_paged(const dsa_config_t *cfg, const uint8_t *q_idx8,
+                                                      const float *q_scale, const float *w, const uint8_t *k8_pool,
+                                                      const float *k_scale_pool, const int32_t *q_pos,
+                                                      const dsa_bf16_t *const *q, const uint8_t *const *kv8_pools,
+                                                      int n_layers, const dsa_pages_t *pages, int B, int Q, int T,
+                                                      dsa_bf16_t *const *out, int32_t *idx_out, void *ws,
+                                                      size_t ws_bytes, dsa_stream_t stream);
+
 /* Sets the time limit of the library's bounded device-side waits (an
  * mbarrier phase a kernel waits on: a tile landing, an MMA completing, a peer
  * warp's arrival), in nanoseconds of the GPU's global timer, for every kernel

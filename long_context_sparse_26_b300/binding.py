@@ -25,7 +25,9 @@ EXPORTS = ("dsa_config_default", "dsa_workspace_bytes", "dsa_indexer_scores", "d
            "dsa_status_string", "dsa_get_device_error", "dsa_sparse_mla_attn_noalloc",
            "dsa_indexer_scores_paged", "dsa_sparse_mla_attn_paged", "dsa_indexshare_group_forward_paged",
            "dsa_indexer_scores_fp8", "dsa_indexshare_group_forward_fp8", "dsa_sparse_mla_attn_fp8",
-           "dsa_indexshare_group_forward_fp8kv", "dsa_set_wait_limit_ns", "dsa_sparse_mla_attn_shared")
+           "dsa_indexshare_group_forward_fp8kv", "dsa_set_wait_limit_ns", "dsa_sparse_mla_attn_shared",
+           "dsa_indexer_scores_fp8_paged", "dsa_sparse_mla_attn_fp8_paged", "dsa_indexshare_group_forward_fp8_paged",
+           "dsa_indexshare_group_forward_fp8kv_paged")
 
 FP8_LATENT_ROW_BYTES = 656  # 512 E4M3 codes, 4 fp32 group scales, 64 bf16 RoPE dims
 
@@ -84,6 +86,11 @@ def lib() -> ctypes.CDLL:
                                                        ctypes.POINTER(_VP), _I, _I, _I, _I, ctypes.POINTER(_VP),
                                                        _VP, _VP, _SZ, _VP]
         L.dsa_sparse_mla_attn_fp8.argtypes = [_CFG, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP, _SZ, _VP]
+        L.dsa_indexer_scores_fp8_paged.argtypes = [_CFG, _VP, _VP, _VP, _VP, _VP, _PG, _VP, _I, _I, _I, _VP, _VP]
+        L.dsa_sparse_mla_attn_fp8_paged.argtypes = [_CFG, _VP, _VP, _PG, _VP, _I, _I, _I, _VP, _VP, _VP, _SZ, _VP]
+        for name in ("dsa_indexshare_group_forward_fp8_paged", "dsa_indexshare_group_forward_fp8kv_paged"):
+            getattr(L, name).argtypes = [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(_VP), ctypes.POINTER(_VP),
+                                         _I, _PG, _I, _I, _I, ctypes.POINTER(_VP), _VP, _VP, _SZ, _VP]
         L.dsa_indexshare_group_forward_fp8kv.argtypes = [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(_VP),
                                                          ctypes.POINTER(_VP), _I, _I, _I, _I, ctypes.POINTER(_VP),
                                                          _VP, _VP, _SZ, _VP]
@@ -93,7 +100,8 @@ def lib() -> ctypes.CDLL:
                      "dsa_indexshare_group_forward_paged", "dsa_indexer_scores_fp8",
                      "dsa_indexshare_group_forward_fp8", "dsa_sparse_mla_attn_fp8",
                      "dsa_indexshare_group_forward_fp8kv", "dsa_set_wait_limit_ns",
-                     "dsa_sparse_mla_attn_shared"):
+                     "dsa_sparse_mla_attn_shared", "dsa_indexer_scores_fp8_paged", "dsa_sparse_mla_attn_fp8_paged",
+                     "dsa_indexshare_group_forward_fp8_paged", "dsa_indexshare_group_forward_fp8kv_paged"):
             getattr(L, name).restype = ctypes.c_int
         L.dsa_get_device_error.argtypes = [_VP]
         L.dsa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
@@ -389,3 +397,83 @@ def indexshare_group_forward_fp8kv(cfg, q8, q_scale, w, k8, k_scale, q_pos, qs, 
                                                     _p(k_scale), _p(q_pos), qa, ka, n, B, Q, T, oa, _p(idx_out),
                                                     _p(ws), 0 if ws is None else ws.numel(), _s(stream)),
            "dsa_indexshare_group_forward_fp8kv")
+
+
+def _pages_of_pool(block_table: torch.Tensor, num_pages: int, page_size: int) -> DsaPages:
+    _need(block_table, "block_table", torch.int32, 2)
+    return DsaPages(block_table.data_ptr(), num_pages, page_size, block_table.shape[1])
+
+
+def indexer_scores_fp8_paged(cfg, q8, q_scale, w, k8_pool, k_scale_pool, block_table, q_pos, scores, stream=None):
+    """indexer_scores_fp8 over a paged FP8 key cache: k8_pool [num_pages, page_size, 128] u8 and
+    k_scale_pool [num_pages, page_size] f32 sharing block_table; T = scores.shape[2]."""
+    _need(q8, "q8", torch.uint8, 4); _need(q_scale, "q_scale", torch.float32, 3); _need(w, "w", torch.float32, 3)
+    _need(k8_pool, "k8_pool", torch.uint8, 3); _need(k_scale_pool, "k_scale_pool", torch.float32, 2)
+    _need(q_pos, "q_pos", torch.int32, 2); _need(scores, "scores", torch.float32, 3)
+    if k_scale_pool.shape != k8_pool.shape[:2]:
+        raise ValueError("the scale pool must have the code pool's pages")
+    pg = _pages_of_pool(block_table, k8_pool.shape[0], k8_pool.shape[1])
+    B, Q, T = q8.shape[0], q8.shape[1], scores.shape[2]
+    _check(lib().dsa_indexer_scores_fp8_paged(ctypes.byref(cfg), _p(q8), _p(q_scale), _p(w), _p(k8_pool),
+                                              _p(k_scale_pool), ctypes.byref(pg), _p(q_pos), B, Q, T, _p(scores),
+                                              _s(stream)), "dsa_indexer_scores_fp8_paged")
+
+
+def sparse_mla_attn_fp8_paged(cfg, q, kv8_pool, block_table, idx, out, T, lse=None, ws=None, stream=None):
+    """sparse_mla_attn_fp8 over a paged FP8 latent cache kv8_pool [num_pages, page_size, 656] u8 of context T."""
+    _need(q, "q", torch.bfloat16, 4); _need_fp8_latent(kv8_pool, "kv8_pool"); _need(idx, "idx", torch.int32, 3)
+    _need(out, "out", torch.bfloat16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    pg = _pages_of_pool(block_table, kv8_pool.shape[0], kv8_pool.shape[1])
+    B, Q = q.shape[0], q.shape[1]
+    _check(lib().dsa_sparse_mla_attn_fp8_paged(ctypes.byref(cfg), _p(q), _p(kv8_pool), ctypes.byref(pg), _p(idx), B,
+                                               Q, T, _p(out), _p(lse), _p(ws), 0 if ws is None else ws.numel(),
+                                               _s(stream)), "dsa_sparse_mla_attn_fp8_paged")
+
+
+def _group_fp8_paged(fn, what, cfg, q8, q_scale, w, k8_pool, k_scale_pool, q_pos, qs, kv_pools, block_table, T, outs,
+                     idx_out, ws, stream, fp8_kv):
+    _need(q8, "q8", torch.uint8, 4); _need(q_scale, "q_scale", torch.float32, 3); _need(w, "w", torch.float32, 3)
+    _need(k8_pool, "k8_pool", torch.uint8, 3); _need(k_scale_pool, "k_scale_pool", torch.float32, 2)
+    _need(q_pos, "q_pos", torch.int32, 2)
+    if k_scale_pool.shape != k8_pool.shape[:2]:
+        raise ValueError("the scale pool must have the code pool's pages")
+    n = len(qs)
+    if len(kv_pools) != n or len(outs) != n:
+        raise ValueError("qs, kv_pools and outs must have one tensor per layer")
+    for i in range(n):
+        _need(qs[i], f"q[{i}]", torch.bfloat16, 4)
+        if fp8_kv:
+            _need_fp8_latent(kv_pools[i], f"kv8_pool[{i}]")
+        else:
+            _need(kv_pools[i], f"kv_pool[{i}]", torch.bfloat16, 3)
+        _need(outs[i], f"out[{i}]", torch.bfloat16, 4)
+        if kv_pools[i].shape[:2] != k8_pool.shape[:2]:
+            raise ValueError("every pool must have the key pool's pages")
+    if idx_out is not None:
+        _need(idx_out, "idx_out", torch.int32, 3)
+    pg = _pages_of_pool(block_table, k8_pool.shape[0], k8_pool.shape[1])
+    B, Q = q8.shape[0], q8.shape[1]
+    arr = _VP * n
+    qa = arr(*[t.data_ptr() for t in qs])
+    ka = arr(*[t.data_ptr() for t in kv_pools])
+    oa = arr(*[t.data_ptr() for t in outs])
+    _check(fn(ctypes.byref(cfg), _p(q8), _p(q_scale), _p(w), _p(k8_pool), _p(k_scale_pool), _p(q_pos), qa, ka, n,
+              ctypes.byref(pg), B, Q, T, oa, _p(idx_out), _p(ws), 0 if ws is None else ws.numel(), _s(stream)), what)
+
+
+def indexshare_group_forward_fp8_paged(cfg, q8, q_scale, w, k8_pool, k_scale_pool, q_pos, qs, kv_pools, block_table,
+                                       T, outs, idx_out=None, ws=None, stream=None):
+    """One IndexShare group with paged FP8 indexer caches and paged bf16 latent pools (one block table)."""
+    _group_fp8_paged(lib().dsa_indexshare_group_forward_fp8_paged, "dsa_indexshare_group_forward_fp8_paged", cfg, q8,
+                     q_scale, w, k8_pool, k_scale_pool, q_pos, qs, kv_pools, block_table, T, outs, idx_out, ws,
+                     stream, False)
+
+
+def indexshare_group_forward_fp8kv_paged(cfg, q8, q_scale, w, k8_pool, k_scale_pool, q_pos, qs, kv8_pools,
+                                         block_table, T, outs, idx_out=None, ws=None, stream=None):
+    """One IndexShare group with paged FP8 indexer caches and paged FP8 latent pools (one block table)."""
+    _group_fp8_paged(lib().dsa_indexshare_group_forward_fp8kv_paged, "dsa_indexshare_group_forward_fp8kv_paged", cfg,
+                     q8, q_scale, w, k8_pool, k_scale_pool, q_pos, qs, kv8_pools, block_table, T, outs, idx_out, ws,
+                     stream, True)

@@ -69,8 +69,8 @@ bool device_state(DeviceState **out) {
                                dsa::mla::kSmemBytes) == cudaSuccess;
     ok &= cudaFuncSetAttribute(dsa::topk::topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dsa::topk::kSelectSmem) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(dsa::topk::topk_chunk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dsa::topk::kSelectSmem) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::topk::topk_chunk_scan_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::topk::kScanSelectSmem) == cudaSuccess;
     if (!ok) return false;
     if (g_encode == nullptr) {
       void *fn = nullptr;
@@ -211,7 +211,7 @@ AttnShape attn_shape(long long rowsL, int K, int sms) {
 }
 
 struct Layout {
-  size_t scores = 0, ghist = 0, plan = 0, counts = 0, cand = 0, idx = 0, part_o = 0, part_ml = 0, total = 0;
+  size_t scores = 0, ghist = 0, done = 0, counts = 0, cand = 0, idx = 0, part_o = 0, part_ml = 0, total = 0;
   TopkShape ts;
 };
 
@@ -232,15 +232,15 @@ Layout layout(int B, int Q, int T, int n_layers, int K, int sms) {
   size_t off = 0;
   L.scores = off;  // offset 0: a group call leaves its scores at the start of the workspace (dsa.h)
   off = align_up(off + static_cast<size_t>(rows) * T * sizeof(float), 256);
-  // chunked top-k: digit histograms, row plans and per-chunk candidate
-  // counts (zeroed by one memset, so they are adjacent), then room for T
-  // candidates per row
+  // chunked top-k: digit-0 histograms and per-row chunk tickets (zeroed by
+  // one memset, so they are adjacent), per-chunk candidate counts, then room
+  // for T candidates per row
   L.ghist = off;
   if (L.ts.nchunk > 1) off += static_cast<size_t>(rows) * dsa::topk::kGhistStride * 4;
-  L.plan = off;
-  if (L.ts.nchunk > 1) off += static_cast<size_t>(rows) * 4 * 4;
+  L.done = off;
+  if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(rows) * 4, 256);
   L.counts = off;
-  if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(rows) * L.ts.nchunk * 2 * 4, 256);
+  if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(rows) * L.ts.nchunk * 4, 256);
   L.cand = off;
   if (L.ts.nchunk > 1) off = align_up(off + static_cast<size_t>(rows) * T * 8, 256);
   L.idx = off;
@@ -325,7 +325,7 @@ dsa_status_t launch_indexer(const DeviceState &dev, const void *q_idx, const flo
 // it counts the digit-0 histogram itself).
 dsa_status_t clear_topk_state(const Layout &L, uint8_t *ws, cudaStream_t stream) {
   if (L.ts.nchunk <= 1) return DSA_OK;
-  return cudaMemsetAsync(ws + L.ghist, 0, L.cand - L.ghist, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return cudaMemsetAsync(ws + L.ghist, 0, L.counts - L.ghist, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 // hist_done: the digit-0 histograms were already counted (by the indexer).
@@ -345,7 +345,7 @@ dsa_status_t launch_topk(const Layout &L, uint8_t *ws, const float *scores, cons
   p.chunk = L.ts.chunk;
   p.nchunk = L.ts.nchunk;
   p.ghist = reinterpret_cast<uint32_t *>(ws + L.ghist);
-  p.plan = reinterpret_cast<uint32_t *>(ws + L.plan);
+  p.done = reinterpret_cast<uint32_t *>(ws + L.done);
   p.counts = reinterpret_cast<uint32_t *>(ws + L.counts);
   p.cand = reinterpret_cast<uint64_t *>(ws + L.cand);
   p.idx = idx;
@@ -354,9 +354,7 @@ dsa_status_t launch_topk(const Layout &L, uint8_t *ws, const float *scores, cons
     if (clear_topk_state(L, ws, stream) != DSA_OK) return DSA_ERR_CUDA;
     topk_chunk_hist_kernel<<<grid, kThreads, 0, stream>>>(p);
   }
-  topk_chunk_scan_kernel<1><<<grid, kThreads, 0, stream>>>(p);
-  topk_chunk_scan_kernel<2><<<grid, kThreads, 0, stream>>>(p);
-  topk_chunk_select_kernel<<<rows, kThreads, kSelectSmem, stream>>>(p);
+  topk_chunk_scan_select_kernel<<<grid, kThreads, kScanSelectSmem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -370,12 +368,23 @@ dsa_status_t enqueue_attention(const dsa::attn::Params &p, int B, cudaStream_t s
     if (!make_tmap_576(&maps.q[l], p.q[l], static_cast<unsigned long long>(p.rows) * kHeads, kHeads))
       return DSA_ERR_CUDA;
   const long long blocks = static_cast<long long>(p.n_layers) * p.nsplit * p.rows;
-  if (p.kv_fp8)
-    dsa::mla::sparse_mla_tc_kernel<true>
-        <<<static_cast<unsigned>(blocks), dsa::mla::kThreads, dsa::mla::kSmemBytes, stream>>>(maps, p);
-  else
-    dsa::mla::sparse_mla_tc_kernel<false>
-        <<<static_cast<unsigned>(blocks), dsa::mla::kThreads, dsa::mla::kSmemBytes, stream>>>(maps, p);
+  // a programmatic dependent launch: the blocks may start (barriers, tensor
+  // memory, the query panels) while the kernel before them on the stream
+  // finishes; they wait for it (griddepcontrol.wait) before reading idx
+  cudaLaunchConfig_t lc;
+  std::memset(&lc, 0, sizeof(lc));
+  lc.gridDim = dim3(static_cast<unsigned>(blocks));
+  lc.blockDim = dim3(dsa::mla::kThreads);
+  lc.dynamicSmemBytes = dsa::mla::kSmemBytes;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  const cudaError_t e = p.kv_fp8 ? cudaLaunchKernelEx(&lc, dsa::mla::sparse_mla_tc_kernel<true>, maps, p)
+                                 : cudaLaunchKernelEx(&lc, dsa::mla::sparse_mla_tc_kernel<false>, maps, p);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
   if (p.nsplit > 1) {
     const dim3 cgrid(kHeads, static_cast<unsigned>(static_cast<long long>(p.rows) * p.n_layers));
     dsa::attn::combine_kernel<<<cgrid, 128, 0, stream>>>(p);
@@ -742,6 +751,86 @@ dsa_status_t dsa_indexshare_group_forward_fp8kv(const dsa_config_t *cfg, const u
   return group_forward(cfg, q_idx8, w, k_idx8, q_pos, q, reinterpret_cast<const void *const *>(kv8), n_layers, B, Q,
                        T, out, idx_out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr, q_scale,
                        k_scale, true);
+}
+
+dsa_status_t dsa_indexer_scores_fp8_paged(const dsa_config_t *cfg, const uint8_t *q_idx8, const float *q_scale,
+                                          const float *w, const uint8_t *k8_pool, const float *k_scale_pool,
+                                          const dsa_pages_t *pages, const int32_t *q_pos, int B, int Q, int T,
+                                          float *scores, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
+  DSA_TRY(check_sizes(B, Q, T));
+  DSA_TRY(check_pages(pages, B, T));
+  if (!q_idx8 || !q_scale || !w || !k8_pool || !k_scale_pool || !q_pos || !scores) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx8) || !aligned16(q_scale) || !aligned16(w) || !aligned16(k8_pool) ||
+      !aligned16(k_scale_pool) || !aligned16(q_pos) || !aligned16(scores))
+    return DSA_ERR_ALIGNMENT;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  return launch_indexer(*dev, q_idx8, w, k8_pool, q_pos, B, Q, T, scores, reinterpret_cast<cudaStream_t>(stream),
+                        nullptr, pages, q_scale, k_scale_pool);
+}
+
+dsa_status_t dsa_sparse_mla_attn_fp8_paged(const dsa_config_t *cfg, const dsa_bf16_t *q, const uint8_t *kv8_pool,
+                                           const dsa_pages_t *pages, const int32_t *idx, int B, int Q, int T,
+                                           dsa_bf16_t *out, float *lse, void *ws, size_t ws_bytes,
+                                           dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
+  DSA_TRY(check_sizes(B, Q, T));
+  DSA_TRY(check_pages(pages, B, T));
+  if (!q || !kv8_pool || !idx || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv8_pool) || !aligned16(idx) || !aligned16(out) || (lse && !aligned16(lse)) ||
+      (ws && !aligned16(ws)))
+    return DSA_ERR_ALIGNMENT;
+  DeviceState *dev = nullptr;
+  if (!device_state(&dev)) return DSA_ERR_CUDA;
+  const Layout L = layout(B, Q, T, 1, cfg->topk, dev->sms);
+  if (attn_shape(static_cast<long long>(B) * Q, cfg->topk, dev->sms).nsplit > 1 &&
+      (ws == nullptr || ws_bytes < L.total))
+    return DSA_ERR_WORKSPACE;
+  const dsa_bf16_t *qs[1] = {q};
+  const void *kvs[1] = {kv8_pool};
+  dsa_bf16_t *outs[1] = {out};
+  float *lses[1] = {lse};
+  return launch_attention(*dev, L, static_cast<uint8_t *>(ws), qs, kvs, outs, lses, 1, idx, B * Q, Q, T, cfg->topk,
+                          cfg->sm_scale, reinterpret_cast<cudaStream_t>(stream), pages, true);
+}
+
+dsa_status_t dsa_indexshare_group_forward_fp8_paged(const dsa_config_t *cfg, const uint8_t *q_idx8,
+                                                    const float *q_scale, const float *w, const uint8_t *k8_pool,
+                                                    const float *k_scale_pool, const int32_t *q_pos,
+                                                    const dsa_bf16_t *const *q, const dsa_bf16_t *const *kv_pools,
+                                                    int n_layers, const dsa_pages_t *pages, int B, int Q, int T,
+                                                    dsa_bf16_t *const *out, int32_t *idx_out, void *ws,
+                                                    size_t ws_bytes, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
+  DSA_TRY(check_sizes(B, Q, T));
+  DSA_TRY(check_pages(pages, B, T));
+  if (!q_scale || !k_scale_pool) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_scale) || !aligned16(k_scale_pool)) return DSA_ERR_ALIGNMENT;
+  return group_forward(cfg, q_idx8, w, k8_pool, q_pos, q, reinterpret_cast<const void *const *>(kv_pools), n_layers,
+                       B, Q, T, out, idx_out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), pages, q_scale,
+                       k_scale_pool);
+}
+
+dsa_status_t dsa_indexshare_group_forward_fp8kv_paged(const dsa_config_t *cfg, const uint8_t *q_idx8,
+                                                      const float *q_scale, const float *w, const uint8_t *k8_pool,
+                                                      const float *k_scale_pool, const int32_t *q_pos,
+                                                      const dsa_bf16_t *const *q, const uint8_t *const *kv8_pools,
+                                                      int n_layers, const dsa_pages_t *pages, int B, int Q, int T,
+                                                      dsa_bf16_t *const *out, int32_t *idx_out, void *ws,
+                                                      size_t ws_bytes, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (empty_call(B, Q, T)) return DSA_OK;
+  DSA_TRY(check_sizes(B, Q, T));
+  DSA_TRY(check_pages(pages, B, T));
+  if (!q_scale || !k_scale_pool) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_scale) || !aligned16(k_scale_pool)) return DSA_ERR_ALIGNMENT;
+  return group_forward(cfg, q_idx8, w, k8_pool, q_pos, q, reinterpret_cast<const void *const *>(kv8_pools), n_layers,
+                       B, Q, T, out, idx_out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), pages, q_scale,
+                       k_scale_pool, true);
 }
 }  // extern "C"
 

@@ -95,6 +95,7 @@ struct Params {
   const int32_t *block_table;  // [B, max_pages]
   int page_size, max_pages, num_pages;
   // FP8 caches only: row (b,s) of the key cache stands for k8 * k_scale[b*T+s]
+  // (paged: the scales form a [pages, page_size] pool beside the code pool)
   // and head row (b,t,j) of the queries for q8 * q_scale[(b*Q+t)*64+j]
   const float *k_scale;
   const float *q_scale;
@@ -396,9 +397,20 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
     auto prefetch_scale = [&]() {
       if (pc.u < u_end) {
         const int kk = pc.tile * kUnitKeys + key_off;
-        if (kk < p.T)
-          cp_async_4(ks_slot0 + static_cast<uint32_t>((pc.u - u_begin) & (kSD - 1)) * 128u,
-                     p.k_scale + (size_t)pc.b * p.T + kk);
+        if (kk < p.T) {
+          // the key's scale: [B, T] contiguous, or a pool [pages, page_size]
+          // beside the code pool, located through the same block table (a
+          // page outside the pool reads page 0, as the codes do; the
+          // producer reports it)
+          size_t si = (size_t)pc.b * p.T + kk;
+          if (p.block_table != nullptr) {
+            const int page = kk / p.page_size;
+            int phys = __ldg(p.block_table + (size_t)pc.b * p.max_pages + page);
+            phys = (phys < 0 || phys >= p.num_pages) ? 0 : phys;
+            si = (size_t)phys * p.page_size + (kk - page * p.page_size);
+          }
+          cp_async_4(ks_slot0 + static_cast<uint32_t>((pc.u - u_begin) & (kSD - 1)) * 128u, p.k_scale + si);
+        }
       }
       cp_async_commit();
       pc.next(p);

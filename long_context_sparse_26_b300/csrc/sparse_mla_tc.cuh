@@ -294,25 +294,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm->mma2_done, 1);
     sm->abort = 0;
     fence_mbar_init();
+    // the query panels are an input of this call, not of the kernel before:
+    // they load while that kernel may still be running (dependent launch)
+    if (nblk > 0) {
+      prefetch_tensormap(&maps.q[layer]);
+      mbar_arrive_expect_tx(&sm->q_full, kQBytes);
+      for (int pp = 0; pp < kPanels; ++pp)
+        tma_load_2d(sQ + pp * kH * 128, &maps.q[layer], pp * 64, row * kH, &sm->q_full);
+    }
   }
-  if (warp == 0 && lane == 0) prefetch_tensormap(&maps.q[layer]);
   if (warp == kMmaWarp) tmem_alloc(&sm->tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = sm->tmem_slot;
+  // launched as a dependent of the kernel that writes the index set (the
+  // top-k select): nothing below reads idx before that kernel has completed
+  // and its writes are visible (a no-op without such a dependency)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp < kProducerWarps) {
     // ------------------------------------------------------------ producers
-    bool q_issued = false;
-    if (warp == 0 && nblk > 0) {
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&sm->q_full, kQBytes);
-        for (int pp = 0; pp < kPanels; ++pp)
-          tma_load_2d(sQ + pp * kH * 128, &maps.q[layer], pp * 64, row * kH, &sm->q_full);
-      }
-      q_issued = true;
-    }
+    const bool q_issued = warp == 0 && nblk > 0;  // thread 0 issued the query panels
     const bool paged = p.block_table != nullptr;
     constexpr size_t kRowBytes = F8KV ? attn::kF8RowBytes : (kDv + 64) * 2;
     const uint8_t *kvb = reinterpret_cast<const uint8_t *>(p.kv[layer]) + (paged ? 0 : (size_t)b * p.T * kRowBytes);

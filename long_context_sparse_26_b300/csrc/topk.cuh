@@ -30,15 +30,17 @@
 // Two launch shapes:
 //   * many rows (prefill): one block per row does every step in shared memory;
 //   * few long rows (decode): (chunk, row) blocks count step 1 (or it comes
-//     fused from the indexer); then (chunk, row) blocks each derive the row's
-//     plan (b0, need, whether bin b0 is taken whole) from the complete
-//     histogram and do steps 2-3, each writing its candidates in order into
-//     its own chunk's slice of a per-row buffer plus a count, and one block
-//     per row gathers the chunks in order and does step 4.  Passes are
-//     separate launches in stream order; no block waits on another.
-// If a row still has more candidates than the select buffer holds (thousands
-// of exactly equal scores), three exact radix passes over the row and an
-// ordered write replace step 4.
+//     fused from the indexer); then, in one launch, (chunk, row) blocks each
+//     derive the row's plan (b0 and the rank of the k-th key within bin b0)
+//     from the complete histogram and write every score of bin b0 or above,
+//     in position order, into their own chunk's slice of a per-row buffer
+//     with a count, and the block that finishes its row last (an atomic
+//     ticket; no block ever waits on another) does step 4 reading the
+//     slices in place.  Bin b0 is always taken whole there, so these rows
+//     need no second digit and no cap on the candidate count.
+// In the one-block-per-row shape, if a row has more candidates than the
+// select buffer holds (thousands of exactly equal scores), three exact radix
+// passes over the row and an ordered write replace step 4.
 #pragma once
 
 #include "common.cuh"
@@ -521,23 +523,28 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const float *__restr
 }
 
 // --------------------------------------------------------------------------
-// Few long rows: (chunk, row) blocks.  ghist [rows][kBins0 + kBins] (digit 0,
-// then digit 1 within bin b0) must be zero before step 1.  plan [rows][4]
-// holds each row's RowPlan.  cand [rows][T] holds each chunk's candidates at
-// the chunk's own offset; counts [rows][nchunk][2] how many each pass left.
+// Few long rows: (chunk, row) blocks.  ghist [rows][kGhistStride] (digit 0 in
+// the first kBins0 words) and done [rows] must be zero before step 1 (one
+// memset clears both).  cand [rows][T] holds each chunk's candidates at the
+// chunk's own offset; counts [rows][nchunk] how many each chunk left.
 // --------------------------------------------------------------------------
 struct ChunkParams {
   const float *scores;
   const int32_t *q_pos;
   int T, K, rows, chunk, nchunk;
   uint32_t *ghist;
-  uint32_t *plan;
   uint32_t *counts;
+  uint32_t *done;        // per row: chunks of the row that have written their candidates
   uint64_t *cand;
   int32_t *idx;
 };
 
 constexpr int kGhistStride = kBins0 + kBins;  // per-row words of ghist
+// The row's last block copies up to this many candidates into its dynamic
+// shared memory (40 KB: four 512-thread blocks of the scan still fit an SM)
+// and selects there; a row with more reads them in place from L2.
+constexpr int kSelCap = 5120;
+constexpr int kScanSelectSmem = kSelCap * 8;
 
 __global__ void __launch_bounds__(kThreads) topk_chunk_hist_kernel(const ChunkParams p) {
   __shared__ uint32_t hist[kBins0];
@@ -555,104 +562,149 @@ __global__ void __launch_bounds__(kThreads) topk_chunk_hist_kernel(const ChunkPa
     if (hist[i]) atomicAdd(g + i, hist[i]);
 }
 
-__device__ __forceinline__ RowPlan load_plan(const ChunkParams &p, int row) {
-  const uint32_t *pl = p.plan + (size_t)row * 4;
-  RowPlan rp;
-  rp.b0 = pl[0];
-  rp.need1 = pl[1];
-  rp.take_b0 = pl[2] != 0;
-  return rp;
-}
-
-// PASS 1: the chunk's candidates of pass 1 (and, on a two-pass row, its
-// digit-1 histogram of bin b0).  PASS 2 (two-pass rows only): bin b0 at or
-// above sub-bin b1, after the chunk's pass-1 candidates.
-template <int PASS>
-__global__ void __launch_bounds__(kThreads) topk_chunk_scan_kernel(const ChunkParams p) {
-  __shared__ uint32_t hist[kBins];
-  __shared__ Scratch sc;
-  const int row = blockIdx.y, c = blockIdx.x;
-  const int L = visible_length(p.q_pos, row, p.T);
-  const int start = c * p.chunk;
-  if (L <= p.K || start >= L) return;
-  const int end = min(start + p.chunk, L);
-  uint32_t *g1 = p.ghist + (size_t)row * kGhistStride + kBins0;
-  // pass 1: every block of the row derives the row's plan from its complete
-  // digit-0 histogram (the same in each block); chunk 0 records it for the
-  // later kernels
-  RowPlan rp;
-  if (PASS == 1) {
-    rp = plan_row_global(p.ghist + (size_t)row * kGhistStride, static_cast<uint32_t>(p.K), &sc);
-    if (c == 0 && threadIdx.x == 0) {
-      uint32_t *pl = p.plan + (size_t)row * 4;
-      pl[0] = rp.b0;
-      pl[1] = rp.need1;
-      pl[2] = rp.take_b0 ? 1u : 0u;
-    }
-  } else {
-    rp = load_plan(p, row);
-  }
-  if (PASS == 2 && rp.take_b0) return;  // single-pass row
-  uint32_t b1 = 0;
-  if (PASS == 1) {
-    for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
-  } else {
-    for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = g1[i];
-    __syncthreads();
-    find_threshold_bin(hist, rp.need1, &sc);
-    b1 = sc.result[0];
-  }
-  __syncthreads();
-  uint32_t *cnt = p.counts + ((size_t)row * p.nchunk + c) * 2;
-  const uint32_t before = PASS == 1 ? 0u : cnt[0];
-  uint64_t *dst = p.cand + (size_t)row * p.T + start + before;
-  const uint32_t cap = static_cast<uint32_t>(end - start) - before;  // never exceeded: positions are distinct
-  const uint32_t n = scan_ordered<PASS>(p.scores + (size_t)row * p.T, start, end, rp, b1,
-                                        (PASS == 1 && !rp.take_b0) ? hist : nullptr, dst, cap, &sc);
-  if (threadIdx.x == 0) cnt[PASS - 1] = n;
-  if (PASS == 1 && !rp.take_b0) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < kBins; i += kThreads)
-      if (hist[i]) atomicAdd(g1 + i, hist[i]);
-  }
-}
-
-__global__ void __launch_bounds__(kThreads) topk_chunk_select_kernel(const ChunkParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ Scratch sc;
-  const SmemViews s = smem_views(smem);
-  const int row = blockIdx.x;
-  const int L = visible_length(p.q_pos, row, p.T);
-  int32_t *out = p.idx + (size_t)row * p.K;
-  if (write_short_row(L, p.K, out)) return;
-  const RowPlan rp = load_plan(p, row);
-  // chunk c holds counts[c][0] (+ counts[c][1] on a two-pass row) candidates;
-  // their offsets in the gathered list are a prefix sum (nchunk <= kThreads)
-  const int nvalid = (L + p.chunk - 1) / p.chunk;
-  uint32_t *coff = reinterpret_cast<uint32_t *>(s.sortbuf);  // [kThreads] chunk offsets, then [kThreads] counts
-  uint32_t mine = 0;
-  if (static_cast<int>(threadIdx.x) < nvalid) {
-    const uint32_t *cnt = p.counts + ((size_t)row * p.nchunk + threadIdx.x) * 2;
-    mine = cnt[0] + (rp.take_b0 ? 0u : cnt[1]);
-  }
-  uint32_t n;
-  const uint32_t off = block_exclusive_sum(mine, &n, &sc);
-  coff[threadIdx.x] = off;
-  coff[kThreads + threadIdx.x] = mine;
-  __syncthreads();
-  if (n > static_cast<uint32_t>(kSmemCand)) {
-    row_select_multipass(p.scores + (size_t)row * p.T, L, p.K, out, s.hist, &sc);
-    return;
-  }
-  // one warp per chunk copies its run into place
+// The candidates of a row, read in place from their chunk slices (written by
+// other blocks of this launch: L2 loads, never a stale L1 line).  Warp w
+// walks chunks w, w + 16, ...; ccnt[c] is chunk c's count.
+template <typename F>
+__device__ __forceinline__ void for_each_candidate(const uint64_t *crow, int chunk, int nvalid, const uint32_t *ccnt,
+                                                   F &&f) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int c = warp; c < nvalid; c += kThreads / 32) {
-    const uint64_t *src = p.cand + (size_t)row * p.T + (size_t)c * p.chunk;
-    const uint32_t o = coff[c], m = coff[kThreads + c];
-    for (uint32_t i = lane; i < m; i += 32) s.cand[o + i] = src[i];
+    const uint64_t *src = crow + (size_t)c * chunk;
+    const uint32_t m = ccnt[c];
+    for (uint32_t i = lane; i < m; i += 32) f(__ldcg(src + i));
+  }
+}
+
+// Step 4 over the candidates in their chunk slices: the exact k-th composite
+// tau by radix passes within bin b0 (the plan fixes digit 0 of the k-th
+// composite and its rank need1 within the bin), then the k positions with
+// composite >= tau written in position order (chunks in order, each chunk's
+// candidates in order).
+__device__ void select_from_chunks(const uint64_t *crow, int chunk, int nvalid, const uint32_t *ccnt,
+                                   const RowPlan &rp, int K, uint32_t *hist, uint32_t *qoff, int32_t *out,
+                                   Scratch *sc) {
+  uint32_t need = rp.need1;
+  uint64_t prefix = static_cast<uint64_t>(rp.b0) << 51, known = 0x1FFFull << 51;
+  for (int shift = 40;; shift -= 11) {
+    const int sh = shift < 0 ? 0 : shift;
+    const int width = shift < 0 ? 11 + shift : 11;
+    const uint64_t dmask = (1ull << width) - 1ull;
+    for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    for_each_candidate(crow, chunk, nvalid, ccnt, [&](uint64_t v) {
+      if ((v & known) == prefix) atomicAdd(&hist[static_cast<uint32_t>((v >> sh) & dmask)], 1u);
+    });
+    __syncthreads();
+    find_threshold_bin(hist, need, sc);
+    const uint32_t bin = sc->result[0], rem = sc->result[1], cnt = sc->result[2];
+    __syncthreads();
+    prefix |= static_cast<uint64_t>(bin) << sh;
+    known |= dmask << sh;
+    if (rem == cnt || sh == 0) break;  // the whole bin is taken: every lower bit may be zero
+    need = rem;
+  }
+  const uint64_t tau = prefix;
+  // winners per chunk, their offsets in the output, then an ordered write
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int c = warp; c < nvalid; c += kThreads / 32) {
+    const uint64_t *src = crow + (size_t)c * chunk;
+    const uint32_t m = ccnt[c];
+    uint32_t n = 0;
+    for (uint32_t i = lane; i < m; i += 32) n += __ldcg(src + i) >= tau ? 1u : 0u;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+    if (lane == 0) qoff[c] = n;
   }
   __syncthreads();
-  finish_row(s.cand, n, p.K, rp, rp.take_b0, s, out, &sc);
+  uint32_t tot;
+  const uint32_t mine = static_cast<int>(threadIdx.x) < nvalid ? qoff[threadIdx.x] : 0u;
+  const uint32_t before = block_exclusive_sum(mine, &tot, sc);
+  if (static_cast<int>(threadIdx.x) < nvalid) qoff[threadIdx.x] = before;
+  __syncthreads();
+  for (int c = warp; c < nvalid; c += kThreads / 32) {
+    const uint64_t *src = crow + (size_t)c * chunk;
+    const uint32_t m = ccnt[c];
+    uint32_t base = qoff[c];
+    for (uint32_t i0 = 0; i0 < m; i0 += 32) {
+      const uint32_t i = i0 + lane;
+      const uint64_t v = i < m ? __ldcg(src + i) : 0ull;
+      const bool sel = i < m && v >= tau;
+      const uint32_t bal = __ballot_sync(0xffffffffu, sel);
+      const uint32_t slot = base + __popc(bal & ((1u << lane) - 1u));
+      if (sel && slot < static_cast<uint32_t>(K)) out[slot] = composite_pos(v);
+      base += __popc(bal);
+    }
+  }
+}
+
+// Steps 2-4 in one launch.  Every (chunk, row) block derives the row's plan
+// from its complete digit-0 histogram and writes, in position order, the
+// chunk's scores in bin b0 or above (all of bin b0: no second digit) into
+// the chunk's slice, with their count.  The block that finishes its row last
+// (a ticket taken after the block's writes are fenced; no block waits on
+// another) selects the row's k winners from the slices.
+__global__ void __launch_bounds__(kThreads, 4) topk_chunk_scan_select_kernel(const ChunkParams p) {
+  extern __shared__ __align__(16) uint64_t s_cand[];  // kSelCap
+  __shared__ uint32_t hist[kBins];
+  __shared__ uint32_t ccnt[kThreads];
+  __shared__ uint32_t qoff[kThreads];
+  __shared__ Scratch sc;
+  __shared__ int last;
+  const int row = blockIdx.y, c = blockIdx.x;
+  const int L = visible_length(p.q_pos, row, p.T);
+  int32_t *out = p.idx + (size_t)row * p.K;
+  if (L <= p.K) {
+    if (c == 0) write_short_row(L, p.K, out);
+    return;
+  }
+  const int start = c * p.chunk;
+  if (start >= L) return;
+  const int end = min(start + p.chunk, L);
+  RowPlan rp = plan_row_global(p.ghist + (size_t)row * kGhistStride, static_cast<uint32_t>(p.K), &sc);
+  rp.take_b0 = true;
+  const uint64_t *crow = p.cand + (size_t)row * p.T;
+  // never exceeded: positions are distinct
+  const uint32_t n = scan_ordered<1>(p.scores + (size_t)row * p.T, start, end, rp, 0, nullptr,
+                                     p.cand + (size_t)row * p.T + start, static_cast<uint32_t>(end - start), &sc);
+  if (threadIdx.x == 0) p.counts[(size_t)row * p.nchunk + c] = n;
+  // the kernel after this one (the attention, a dependent launch) may start
+  // its prologue on free SMs now; it reads idx only once this grid is complete
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the row's ticket, once this block's candidates and count are visible
+  __threadfence();
+  __syncthreads();
+  const int nvalid = (L + p.chunk - 1) / p.chunk;
+  if (threadIdx.x == 0) last = atomicAdd(p.done + row, 1u) == static_cast<uint32_t>(nvalid - 1) ? 1 : 0;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();  // every other chunk's writes, fenced before its ticket, are visible now
+  const uint32_t mc = static_cast<int>(threadIdx.x) < nvalid ? __ldcg(p.counts + (size_t)row * p.nchunk + threadIdx.x) : 0u;
+  uint32_t ncand;
+  const uint32_t off = block_exclusive_sum(mc, &ncand, &sc);
+  ccnt[threadIdx.x] = mc;
+  qoff[threadIdx.x] = off;
+  __syncthreads();
+  if (ncand > static_cast<uint32_t>(kSelCap)) {
+    select_from_chunks(crow, p.chunk, nvalid, ccnt, rp, p.K, hist, qoff, out, &sc);
+    return;
+  }
+  // the chunks, in order, into shared memory (one pass over L2, every load
+  // independent: entry i of the gathered list belongs to the last chunk whose
+  // offset is <= i), then every radix pass and the ordered write in shared memory
+  for (uint32_t i = threadIdx.x; i < ncand; i += kThreads) {
+    int lo = 0, hi = nvalid;  // first chunk with offset > i is hi
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (qoff[mid] <= i) lo = mid + 1; else hi = mid;
+    }
+    const int cc = lo - 1;
+    s_cand[i] = __ldcg(crow + (size_t)cc * p.chunk + (i - qoff[cc]));
+  }
+  __syncthreads();
+  const uint64_t tau = select_threshold(s_cand, ncand, rp.need1, hist, &sc, static_cast<uint64_t>(rp.b0) << 51,
+                                        0x1FFFull << 51, 40);
+  write_ordered(s_cand, ncand, tau, p.K, out, &sc);
 }
 
 }  // namespace topk

@@ -177,3 +177,111 @@ def test_full_decode_1m_fp8kv_sampled():
     ties = _fp8_group_check(wl.DECODE_1M, rows=[(2, 0), (7, 0)], fp8_kv=True)
     print("boundary ties at 1M (fp8 caches):", ties)
     torch.cuda.empty_cache()
+
+
+# --------------------------------------------------------------------------- FP8 caches in pages
+
+@pytest.mark.parametrize("B,Q,T,first,page", [
+    (3, 1, 3001, 3000, 64),     # 256-key units over 64-row pages, ragged last page
+    (2, 1, 5000, 1234, 128),    # a position inside a unit
+    (1, 4, 2500, 2496, 256),    # four queries per group
+])
+def test_fp8_paged_indexer(B, Q, T, first, page):
+    """Paged FP8 key codes and scales equal the contiguous FP8 call bit for bit,
+    and the oracle over the cache the pools stand for."""
+    cfg = dsa.default_config()
+    q8, q_scale, w, k8, k_scale, pos = _fp8_inputs(B, Q, T, first, seed=T + page)
+    (k8_pool, ks_pool), table = wl.paginate([k8, k_scale], page, seed=T)
+    ref = torch.empty(B, Q, T, device=DEV)
+    got = torch.full((B, Q, T), float("nan"), device=DEV)
+    dsa.indexer_scores_fp8(cfg, q8, q_scale, w, k8, k_scale, pos, ref)
+    dsa.indexer_scores_fp8_paged(cfg, q8, q_scale, w, k8_pool, ks_pool, table, pos, got)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+    tab = table.cpu().numpy()
+    k_o = oracle.gather_pages(oracle.e4m3_to_f64(k8_pool.cpu().numpy()), tab, T) * \
+        oracle.gather_pages(ks_pool.cpu().double().numpy()[..., None], tab, T)
+    ora = oracle.indexer_scores(_decoded(q8, q_scale), f64(w), k_o, pos.cpu().numpy())
+    g = got.cpu().double().numpy()
+    for b in range(B):
+        for t in range(Q):
+            check_scores_row(g[b, t], ora[b, t], int(pos[b, t]))
+
+
+def test_fp8_paged_attention():
+    cfg = dsa.default_config()
+    B, Q, T, page = 2, 2, 9000, 64
+    q = wl.mla_queries(B, Q, 17, 0, DEV)
+    kv8 = wl.to_fp8_latent(wl.latent_cache(B, T, 17, 0, DEV))
+    rng = np.random.default_rng(17)
+    idx = np.full((B, Q, 2048), -1, dtype=np.int32)
+    for b in range(B):
+        for t in range(Q):
+            idx[b, t, :2040] = np.sort(rng.choice(T, 2040, replace=False))
+    idx = torch.from_numpy(idx).to(DEV)
+    (kv8_pool,), table = wl.paginate([kv8], page, seed=17)
+    ws = dsa.alloc_workspace(cfg, B, Q, T, 1)
+    ref = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+    got = torch.empty_like(ref)
+    ref_lse = torch.empty(B, Q, 64, device=DEV)
+    got_lse = torch.empty_like(ref_lse)
+    dsa.sparse_mla_attn_fp8(cfg, q, kv8, idx, ref, ref_lse, ws)
+    dsa.sparse_mla_attn_fp8_paged(cfg, q, kv8_pool, table, idx, got, T, got_lse, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref) and torch.equal(got_lse, ref_lse)
+    kv_o = oracle.fp8_latent_to_f64(oracle.gather_pages(kv8_pool.cpu().numpy(), table.cpu().numpy(), T))
+    O, _ = oracle.sparse_mla_attn(f64(q), kv_o, idx.cpu().numpy(), wl.SM_SCALE)
+    check_attention(f64(got), O)
+
+
+@pytest.mark.parametrize("fp8_kv", [False, True])
+def test_fp8_paged_group(fp8_kv):
+    """The group with paged FP8 indexer caches (and paged bf16 or FP8 latent
+    pools) equals the contiguous FP8 group bit for bit, and the oracle's group
+    over the decoded caches the pools stand for."""
+    import dataclasses
+    B, Q, T, page = 2, 2, 20_000, 128
+    w_ = dataclasses.replace(wl.TINY, name="fp8_paged", B=B, Q=Q, T=T, first_pos=T - Q, seed=91)
+    cfg = dsa.default_config()
+    inp = wl.make_inputs(w_, DEV)
+    q8, q_scale = wl.to_e4m3_rows(inp.q_idx)
+    k8, k_scale = wl.to_e4m3_rows(inp.k_idx)
+    kvs = [wl.to_fp8_latent(kv) for kv in inp.kv] if fp8_kv else inp.kv
+    pools, table = wl.paginate([k8, k_scale] + kvs, page, seed=91)
+    k8_pool, ks_pool, kv_pools = pools[0], pools[1], pools[2:]
+    ws = dsa.alloc_workspace(cfg, B, Q, T, 4)
+    outs_ref = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV) for _ in range(4)]
+    outs_got = [torch.empty_like(o) for o in outs_ref]
+    idx_ref = torch.empty(B, Q, 2048, dtype=torch.int32, device=DEV)
+    idx_got = torch.empty_like(idx_ref)
+    if fp8_kv:
+        dsa.indexshare_group_forward_fp8kv(cfg, q8, q_scale, inp.w, k8, k_scale, inp.q_pos, inp.q, kvs, outs_ref,
+                                           idx_ref, ws)
+        dsa.indexshare_group_forward_fp8kv_paged(cfg, q8, q_scale, inp.w, k8_pool, ks_pool, inp.q_pos, inp.q,
+                                                 kv_pools, table, T, outs_got, idx_got, ws)
+    else:
+        dsa.indexshare_group_forward_fp8(cfg, q8, q_scale, inp.w, k8, k_scale, inp.q_pos, inp.q, kvs, outs_ref,
+                                         idx_ref, ws)
+        dsa.indexshare_group_forward_fp8_paged(cfg, q8, q_scale, inp.w, k8_pool, ks_pool, inp.q_pos, inp.q,
+                                               kv_pools, table, T, outs_got, idx_got, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(idx_got, idx_ref)
+    for a, b in zip(outs_got, outs_ref):
+        assert torch.equal(a, b)
+    tab = table.cpu().numpy()
+    pos = inp.q_pos.cpu().numpy()
+    k_o = oracle.gather_pages(oracle.e4m3_to_f64(k8_pool.cpu().numpy()), tab, T) * \
+        oracle.gather_pages(ks_pool.cpu().double().numpy()[..., None], tab, T)
+    S = oracle.indexer_scores(_decoded(q8, q_scale), f64(inp.w), k_o, pos)
+    o_idx = oracle.topk_select(S, pos, 2048)
+    g_idx = idx_got.cpu().numpy()
+    for b in range(B):
+        for t in range(Q):
+            check_topk_row(g_idx[b, t], o_idx[b, t], S[b, t], int(pos[b, t]), 2048)
+    for layer in range(4):
+        if fp8_kv:
+            kv_o = oracle.fp8_latent_to_f64(oracle.gather_pages(kv_pools[layer].cpu().numpy(), tab, T))
+        else:
+            kv_o = oracle.gather_pages(f64(kv_pools[layer]), tab, T)
+        ref, _ = oracle.sparse_mla_attn(f64(inp.q[layer]), kv_o, g_idx, wl.SM_SCALE)
+        check_attention(f64(outs_got[layer]), ref)
