@@ -29,6 +29,27 @@ constexpr int kMaxDevices = 64;
 constexpr long long kMaxRowsY = 65535;  // grid.y limit for (chunk, row) launches
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Launches `kernel` as a programmatic dependent of the kernel before it on
+// the stream: its blocks may be scheduled while that kernel finishes, and
+// every one of them executes griddepcontrol.wait before reading what that
+// kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args &&...args) {
+  cudaLaunchConfig_t lc;
+  std::memset(&lc, 0, sizeof(lc));
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
+}
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct DeviceState {
@@ -354,7 +375,8 @@ dsa_status_t launch_topk(const Layout &L, uint8_t *ws, const float *scores, cons
     if (clear_topk_state(L, ws, stream) != DSA_OK) return DSA_ERR_CUDA;
     topk_chunk_hist_kernel<<<grid, kThreads, 0, stream>>>(p);
   }
-  topk_chunk_scan_select_kernel<<<grid, kThreads, kScanSelectSmem, stream>>>(p);
+  if (launch_dependent(topk_chunk_scan_select_kernel, grid, dim3(kThreads), kScanSelectSmem, stream, p) != cudaSuccess)
+    return DSA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -371,23 +393,16 @@ dsa_status_t enqueue_attention(const dsa::attn::Params &p, int B, cudaStream_t s
   // a programmatic dependent launch: the blocks may start (barriers, tensor
   // memory, the query panels) while the kernel before them on the stream
   // finishes; they wait for it (griddepcontrol.wait) before reading idx
-  cudaLaunchConfig_t lc;
-  std::memset(&lc, 0, sizeof(lc));
-  lc.gridDim = dim3(static_cast<unsigned>(blocks));
-  lc.blockDim = dim3(dsa::mla::kThreads);
-  lc.dynamicSmemBytes = dsa::mla::kSmemBytes;
-  lc.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  const cudaError_t e = p.kv_fp8 ? cudaLaunchKernelEx(&lc, dsa::mla::sparse_mla_tc_kernel<true>, maps, p)
-                                 : cudaLaunchKernelEx(&lc, dsa::mla::sparse_mla_tc_kernel<false>, maps, p);
+  const dim3 grid(static_cast<unsigned>(blocks)), block(dsa::mla::kThreads);
+  const cudaError_t e =
+      p.kv_fp8 ? launch_dependent(dsa::mla::sparse_mla_tc_kernel<true>, grid, block, dsa::mla::kSmemBytes, stream, maps, p)
+               : launch_dependent(dsa::mla::sparse_mla_tc_kernel<false>, grid, block, dsa::mla::kSmemBytes, stream, maps,
+                                  p);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   if (p.nsplit > 1) {
     const dim3 cgrid(kHeads, static_cast<unsigned>(static_cast<long long>(p.rows) * p.n_layers));
-    dsa::attn::combine_kernel<<<cgrid, 128, 0, stream>>>(p);
+    if (launch_dependent(dsa::attn::combine_kernel, cgrid, dim3(128), 0, stream, p) != cudaSuccess)
+      return DSA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

@@ -51,6 +51,9 @@ struct Params {
 // Merges the splits of one (layer, row, head): O = sum_s 2^(m_s - M) O_s /
 // sum_s 2^(m_s - M) l_s, lse = (M + log2(sum)) * ln 2.  128 threads x 4 dims.
 __global__ void __launch_bounds__(128) combine_kernel(const Params p) {
+  // launched as a dependent of the attention kernel: its partials are
+  // complete and visible once this returns
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int head = blockIdx.x;
   const size_t rowL = blockIdx.y;
   const int layer = static_cast<int>(rowL / p.rows);

@@ -651,6 +651,9 @@ __global__ void __launch_bounds__(kThreads, 4) topk_chunk_scan_select_kernel(con
   __shared__ uint32_t qoff[kThreads];
   __shared__ Scratch sc;
   __shared__ int last;
+  // launched as a dependent of the indexer: its scores and histograms are
+  // complete and visible once this returns
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int row = blockIdx.y, c = blockIdx.x;
   const int L = visible_length(p.q_pos, row, p.T);
   int32_t *out = p.idx + (size_t)row * p.K;
@@ -699,8 +702,13 @@ __global__ void __launch_bounds__(kThreads, 4) topk_chunk_scan_select_kernel(con
       if (qoff[mid] <= i) lo = mid + 1; else hi = mid;
     }
     const int cc = lo - 1;
-    s_cand[i] = __ldcg(crow + (size_t)cc * p.chunk + (i - qoff[cc]));
+    // an asynchronous 8-byte copy: no load waits for another
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(s_cand + i)),
+                 "l"(crow + (size_t)cc * p.chunk + (i - qoff[cc]))
+                 : "memory");
   }
+  cp_async_commit();
+  cp_async_wait<0>();
   __syncthreads();
   const uint64_t tau = select_threshold(s_cand, ncand, rp.need1, hist, &sc, static_cast<uint64_t>(rp.b0) << 51,
                                         0x1FFFull << 51, 40);
