@@ -51,10 +51,10 @@
 //              O^T chunk c.
 // Tensor memory: O^T in columns 0-255 (chunk c at 64c); the two S partials in
 // two window buffers of kKeys columns each, from 256 and from 384.
-// The epilogue stages the block's result in the (then idle) gather buffers
-// and writes it with coalesced 16-byte stores: bf16 and normalised with one
-// split, else the unnormalised fp32 partial plus (reference max, sum) per
-// head for the combine kernel.
+// The epilogue writes the block's result straight from tensor memory (lane =
+// dim, so each head's stores from a warp are 32 consecutive dims): bf16 and
+// normalised with one split, else the unnormalised fp32 partial plus
+// (reference max, sum) per head for the combine kernel.
 #pragma once
 
 #include "common.cuh"
@@ -779,8 +779,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) sm->status[0][w4] = ok ? 1 : 0;
     named_bar_sync(1, 128);
     ok = sm->status[0][0] && sm->status[0][1] && sm->status[0][2] && sm->status[0][3];
-    // After the last GEMM 2 every gather and MMA of this block is complete, so
-    // the stage buffers are free; on an abort they may not be, so stay out.
+    // After the last GEMM 2 every MMA into O^T is complete; on an abort it
+    // may not be, so its tensor memory is not read.
     const size_t rowL = (size_t)layer * p.rows + row;
     const bool one = p.nsplit == 1;
     if (owner) {
@@ -797,33 +797,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int tid = threadIdx.x - 32 * kSoftmaxWarp0;  // 0..127
     if (ok && nblk > 0) {
+      // straight from tensor memory to global memory: lane = dim, so for each
+      // head a warp's stores cover 32 consecutive dims (coalesced)
       tc_fence_after();
+      float *po = one ? nullptr : p.part_o + ((rowL * p.nsplit + split) * kH) * kDv;
+      __nv_bfloat16 *bo = one ? p.out[layer] + (size_t)row * kH * kDv : nullptr;
 #pragma unroll 1
       for (int c = 0; c < kDv / 128; ++c) {
         const int d = c * 128 + q4 * 32 + lane;
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32_nowait(tmem_base + lane_addr + kOCol + c * 64, r0);
+        tmem_ld_32x32b_x32_nowait(tmem_base + lane_addr + kOCol + c * 64 + 32, r1);
+        tmem_wait_ld();
+        if (one) {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32_nowait(tmem_base + lane_addr + kOCol + c * 64 + hh * 32, r);
-          tmem_wait_ld();
-          if (one) {
-            __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sK);
+          for (int i = 0; i < 32; ++i) {
+            bo[i * kDv + d] = __float2bfloat16_rn(__uint_as_float(r0[i]) * inv_l[i]);
+            bo[(32 + i) * kDv + d] = __float2bfloat16_rn(__uint_as_float(r1[i]) * inv_l[32 + i]);
+          }
+        } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              stg[(hh * 32 + i) * kDv + d] = __float2bfloat16_rn(__uint_as_float(r[i]) * inv_l[hh * 32 + i]);
-          } else {
-            float *stg = reinterpret_cast<float *>(sK);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) stg[(hh * 32 + i) * kDv + d] = __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i) {
+            po[i * kDv + d] = __uint_as_float(r0[i]);
+            po[(32 + i) * kDv + d] = __uint_as_float(r1[i]);
           }
         }
       }
-      named_bar_sync(1, 128);
-      const uint4 *src = reinterpret_cast<const uint4 *>(sK);
-      uint4 *dst = one ? reinterpret_cast<uint4 *>(p.out[layer] + (size_t)row * kH * kDv)
-                       : reinterpret_cast<uint4 *>(p.part_o + ((rowL * p.nsplit + split) * kH) * kDv);
-      const int n16 = one ? kH * kDv * 2 / 16 : kH * kDv * 4 / 16;
-      for (int i = tid; i < n16; i += 128) dst[i] = src[i];
     } else {
       // no index in this slice, or the block gave up: zeros
       uint4 *dst = one ? reinterpret_cast<uint4 *>(p.out[layer] + (size_t)row * kH * kDv)
