@@ -84,6 +84,15 @@ bool device_state(DeviceState **out) {
     ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<4, true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dsa::indexer::Cfg<4, true>::kSmemBytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<1, true, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::indexer::Cfg<1, true>::kSmemBytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<2, true, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::indexer::Cfg<2, true>::kSmemBytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<4, true, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dsa::indexer::Cfg<4, true>::kSmemBytes) == cudaSuccess;
     ok &= cudaFuncSetAttribute(dsa::mla::sparse_mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dsa::mla::kSmemBytes) == cudaSuccess;
     ok &= cudaFuncSetAttribute(dsa::mla::sparse_mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -324,7 +333,14 @@ dsa_status_t launch_indexer(const DeviceState &dev, const void *q_idx, const flo
   using dsa::indexer::Cfg;
   using dsa::indexer::indexer_scores_kernel;
   const unsigned g = static_cast<unsigned>(grid);
-  if (f8) {
+  if (f8 && pages != nullptr) {  // paged FP8 keys: the scales are a paged pool too
+    if (QG == 1)
+      indexer_scores_kernel<1, true, true><<<g, Cfg<1, true>::kThreads, Cfg<1, true>::kSmemBytes, stream>>>(tk, tq, p);
+    else if (QG == 2)
+      indexer_scores_kernel<2, true, true><<<g, Cfg<2, true>::kThreads, Cfg<2, true>::kSmemBytes, stream>>>(tk, tq, p);
+    else
+      indexer_scores_kernel<4, true, true><<<g, Cfg<4, true>::kThreads, Cfg<4, true>::kSmemBytes, stream>>>(tk, tq, p);
+  } else if (f8) {
     if (QG == 1)
       indexer_scores_kernel<1, true><<<g, Cfg<1, true>::kThreads, Cfg<1, true>::kSmemBytes, stream>>>(tk, tq, p);
     else if (QG == 2)

@@ -175,7 +175,9 @@ struct UnitCursor {
   }
 };
 
-template <int QG, bool F8 = false>
+// PGS: FP8 key scales in a paged pool (located through the block table);
+// a separate instantiation, so the contiguous FP8 epilogue pays nothing for it.
+template <int QG, bool F8 = false, bool PGS = false>
 __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
     indexer_scores_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                           const Params p) {
@@ -403,7 +405,7 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
           // page outside the pool reads page 0, as the codes do; the
           // producer reports it)
           size_t si = (size_t)pc.b * p.T + kk;
-          if (p.block_table != nullptr) {
+          if constexpr (PGS) {
             const int page = kk / p.page_size;
             int phys = __ldg(p.block_table + (size_t)pc.b * p.max_pages + page);
             phys = (phys < 0 || phys >= p.num_pages) ? 0 : phys;
