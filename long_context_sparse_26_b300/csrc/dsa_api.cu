@@ -60,6 +60,49 @@ DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// The indexer's instantiations: query-group size x key format (bf16; FP8
+// with contiguous or paged scales; paged bf16 keys are a runtime path of the
+// bf16 kernels), and for one query per group whether the epilogue counts the
+// top-k's histograms.  Each needs its shared-memory attribute set once per
+// device; a launch picks one.
+template <int QG, bool F8, bool PGS, bool HIST>
+struct IndexerInst {
+  using C = dsa::indexer::Cfg<QG, F8, HIST>;
+  static bool set_attr() {
+    return cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<QG, F8, PGS, HIST>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) == cudaSuccess;
+  }
+  static void launch(unsigned grid, const CUtensorMap &tk, const CUtensorMap &tq, const dsa::indexer::Params &p,
+                     cudaStream_t stream) {
+    dsa::indexer::indexer_scores_kernel<QG, F8, PGS, HIST><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tq, p);
+  }
+};
+
+template <bool F8, bool PGS>
+struct IndexerFamily {
+  static bool set_attrs() {
+    return IndexerInst<1, F8, PGS, false>::set_attr() && IndexerInst<1, F8, PGS, true>::set_attr() &&
+           IndexerInst<2, F8, PGS, false>::set_attr() && IndexerInst<4, F8, PGS, false>::set_attr();
+  }
+  // hist: QG == 1 only
+  static void launch(int QG, bool hist, unsigned grid, const CUtensorMap &tk, const CUtensorMap &tq,
+                     const dsa::indexer::Params &p, cudaStream_t stream) {
+    if (QG == 1 && hist)
+      IndexerInst<1, F8, PGS, true>::launch(grid, tk, tq, p, stream);
+    else if (QG == 1)
+      IndexerInst<1, F8, PGS, false>::launch(grid, tk, tq, p, stream);
+    else if (QG == 2)
+      IndexerInst<2, F8, PGS, false>::launch(grid, tk, tq, p, stream);
+    else
+      IndexerInst<4, F8, PGS, false>::launch(grid, tk, tq, p, stream);
+  }
+};
+
+bool set_indexer_attrs() {
+  return IndexerFamily<false, false>::set_attrs() && IndexerFamily<true, false>::set_attrs() &&
+         IndexerFamily<true, true>::set_attrs();
+}
+
 // Per-device facts and one-time kernel attributes.  Returns false on a CUDA error.
 bool device_state(DeviceState **out) {
   int dev = 0;
@@ -69,30 +112,7 @@ bool device_state(DeviceState **out) {
   if (!s.attrs_set) {
     if (cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
     bool ok = true;
-    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dsa::indexer::Cfg<1>::kSmemBytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dsa::indexer::Cfg<2>::kSmemBytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dsa::indexer::Cfg<4>::kSmemBytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<1, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dsa::indexer::Cfg<1, true>::kSmemBytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<2, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dsa::indexer::Cfg<2, true>::kSmemBytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<4, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dsa::indexer::Cfg<4, true>::kSmemBytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<1, true, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dsa::indexer::Cfg<1, true>::kSmemBytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<2, true, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dsa::indexer::Cfg<2, true>::kSmemBytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(dsa::indexer::indexer_scores_kernel<4, true, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dsa::indexer::Cfg<4, true>::kSmemBytes) == cudaSuccess;
+    ok &= set_indexer_attrs();
     ok &= cudaFuncSetAttribute(dsa::mla::sparse_mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dsa::mla::kSmemBytes) == cudaSuccess;
     ok &= cudaFuncSetAttribute(dsa::mla::sparse_mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -330,31 +350,14 @@ dsa_status_t launch_indexer(const DeviceState &dev, const void *q_idx, const flo
   p.q_scale = q_scale;
   p.ghist = QG == 1 ? ghist : nullptr;
   const long long grid = p.units < dev.sms ? p.units : dev.sms;
-  using dsa::indexer::Cfg;
-  using dsa::indexer::indexer_scores_kernel;
   const unsigned g = static_cast<unsigned>(grid);
-  if (f8 && pages != nullptr) {  // paged FP8 keys: the scales are a paged pool too
-    if (QG == 1)
-      indexer_scores_kernel<1, true, true><<<g, Cfg<1, true>::kThreads, Cfg<1, true>::kSmemBytes, stream>>>(tk, tq, p);
-    else if (QG == 2)
-      indexer_scores_kernel<2, true, true><<<g, Cfg<2, true>::kThreads, Cfg<2, true>::kSmemBytes, stream>>>(tk, tq, p);
-    else
-      indexer_scores_kernel<4, true, true><<<g, Cfg<4, true>::kThreads, Cfg<4, true>::kSmemBytes, stream>>>(tk, tq, p);
-  } else if (f8) {
-    if (QG == 1)
-      indexer_scores_kernel<1, true><<<g, Cfg<1, true>::kThreads, Cfg<1, true>::kSmemBytes, stream>>>(tk, tq, p);
-    else if (QG == 2)
-      indexer_scores_kernel<2, true><<<g, Cfg<2, true>::kThreads, Cfg<2, true>::kSmemBytes, stream>>>(tk, tq, p);
-    else
-      indexer_scores_kernel<4, true><<<g, Cfg<4, true>::kThreads, Cfg<4, true>::kSmemBytes, stream>>>(tk, tq, p);
-  } else {
-    if (QG == 1)
-      indexer_scores_kernel<1><<<g, Cfg<1>::kThreads, Cfg<1>::kSmemBytes, stream>>>(tk, tq, p);
-    else if (QG == 2)
-      indexer_scores_kernel<2><<<g, Cfg<2>::kThreads, Cfg<2>::kSmemBytes, stream>>>(tk, tq, p);
-    else
-      indexer_scores_kernel<4><<<g, Cfg<4>::kThreads, Cfg<4>::kSmemBytes, stream>>>(tk, tq, p);
-  }
+  const bool hist = p.ghist != nullptr;
+  if (!f8)
+    IndexerFamily<false, false>::launch(QG, hist, g, tk, tq, p, stream);
+  else if (pages == nullptr)
+    IndexerFamily<true, false>::launch(QG, hist, g, tk, tq, p, stream);
+  else  // paged FP8 keys: the scales are a paged pool too
+    IndexerFamily<true, true>::launch(QG, hist, g, tk, tq, p, stream);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -495,6 +498,7 @@ dsa_status_t group_forward(const dsa_config_t *cfg, const void *q_idx, const flo
   float *scores = reinterpret_cast<float *>(wsb + L.scores);
   int32_t *idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(wsb + L.idx);
   // IndexShare: the indexer and top-k run once for the whole group ...
+  // one query per sequence: the indexer counts the top-k's first histogram
   const bool fuse_hist = Q == 1 && L.ts.nchunk > 1;
   if (fuse_hist) DSA_TRY(clear_topk_state(L, wsb, st));
   DSA_TRY(launch_indexer(*dev, q_idx, w, k_idx, q_pos, B, Q, T, scores, st,

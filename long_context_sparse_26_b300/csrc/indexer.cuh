@@ -30,7 +30,11 @@
 // the epilogue warps share one 8192-bin shared-memory histogram and add it
 // to the global one when the block's sequence changes.  The flush is fenced
 // on both sides by an mbarrier every epilogue warp arrives on (a bounded
-// wait, so a block that gives up never strands a warp).
+// wait, so a block that gives up never strands a warp).  With several
+// queries per group the same rounds guard the group's head weights, which
+// the epilogue warps share.  (Counting there too was measured: those
+// epilogues set the kernel's pace, and the count cost more than the
+// top-k's histogram pass it saves.)
 #pragma once
 
 #include "common.cuh"
@@ -44,7 +48,10 @@ constexpr int kTileKeys = 128;                     // UMMA M
 // A key tile is 128 keys x 128 dims.  bf16: two 64-dim panels of 128-byte
 // rows (16 KB each); FP8 (E4M3): one panel, a 128-dim row being 128 bytes.
 // A unit of work (one pipeline stage, one accumulator slot) is kSub tiles.
-template <int QG, bool F8 = false>
+// HIST (one query per group): the epilogue counts the top-k's digit-0
+// histograms; a separate instantiation, so that calls without them pay
+// nothing.
+template <int QG, bool F8 = false, bool HIST = false>
 struct Cfg {
   static constexpr int N = QG * kHeads;                 // UMMA N: 64, 128 or 256
   static constexpr int kPanels = F8 ? 1 : 2;            // 128-byte panels per row
@@ -59,12 +66,15 @@ struct Cfg {
   static constexpr int kABytes = kPanels * kPanelBytes; // per stage: 32 KB
   static constexpr int kHalfBBytes = N * 128;
   static constexpr int kBBytes = kPanels * kHalfBBytes;
-  static constexpr int kStages = F8 ? (QG == 1 ? 5 : 8) : (QG == 1 ? 5 : (QG == 2 ? 5 : 4));
+  // (4 queries, bf16: two stages, measured faster than three or four; the
+  // 256-column tile keeps the epilogue the slower side)
+  static constexpr int kStages = F8 ? (QG == 1 ? 5 : 8) : (QG == 4 ? 2 : 5);
   // with 4 queries the two warps of a quarter split the queries
   static constexpr int kEpiWarps = (QG == 4 || kSub == 2) ? 8 : 4;
   static constexpr int kQPW = QG * 4 * kSub / kEpiWarps;  // queries per epilogue warp
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr int kHistBytes = QG == 1 ? 8192 * 4 : 0;   // the block's digit-0 histogram
+  static_assert(!HIST || QG == 1, "histograms are counted for one query per group");
+  static constexpr int kHistBytes = HIST ? 8192 * 4 : 0;  // the block's digit-0 histogram
   // FP8: each epilogue warp prefetches its keys' scales kScaleDepth units
   // ahead with cp.async, so the load latency never sits between a tile's
   // accumulator and its release
@@ -72,11 +82,16 @@ struct Cfg {
   static constexpr int kScaleBytes = F8 ? kEpiWarps * kScaleDepth * 32 * 4 : 0;
   static constexpr int kAcc = QG == 4 ? 2 : 4;          // accumulator buffers in TMEM
   static constexpr int kTmemCols = (kAcc * kSub * N <= 256) ? 256 : 512;
-  static constexpr int kSmall = 1024 + kEpiWarps * kQPW * kHeads * 4;  // barriers + flags, then per-warp weights
+  // head weights: one query, a copy per epilogue warp (in registers after
+  // the load); several, one copy of the group's weights that the warps share
+  static constexpr bool kWarpWeights = QG == 1;
+  static constexpr int kWBytes = kWarpWeights ? kEpiWarps * kQPW * kHeads * 4 : QG * kHeads * 4;
+  static constexpr int kSmall = 256 + kWBytes;            // barriers + flags, then the weights
   static constexpr int kSmemBytes = 1024 + kStages * kABytes + kBBytes + kSmall + kHistBytes + kScaleBytes;
   static constexpr int kKSteps = F8 ? kDim / 32 : kDim / 16;  // MMA instructions per tile
   static_assert(kSmemBytes <= 232448, "shared memory per block");
   static_assert(kAcc * kSub * N <= kTmemCols, "accumulators must fit the allocation");
+  static_assert((2 * kStages + 2 * kAcc + 4) * 8 + 8 <= 256, "barriers and flags fit their area");
 };
 
 struct Params {
@@ -88,7 +103,7 @@ struct Params {
   int ntiles;            // ceil(T / keys per unit): units of one (sequence, query group)
   long long units;       // B * ngroups * ntiles
   int stream_keys;       // 1: every key tile is read once (evict-first in L2)
-  uint32_t *ghist;       // QG == 1 only, may be null: [B][8192 + 2048], digit-0 histogram in the first 8192
+  uint32_t *ghist;       // HIST only (Q == 1): [B][8192], each row's digit-0 histogram (added to)
   // paged key cache (block_table null: keys are [B, T, 128] contiguous):
   // position s of sequence b is row block_table[b][s / page_size] * page_size
   // + s % page_size of the [pages * page_size, 128] pool; page_size % 64 == 0
@@ -103,37 +118,35 @@ struct Params {
 
 constexpr int kHistBins = 8192;          // digit 0 of the top-k: key bits 31..19
 constexpr int kHistShift = 19;
-constexpr int kHistRowStride = 8192 + 2048;  // per-row words of the global histograms
+constexpr int kHistRowStride = 8192;  // per-row words of the global histograms
 
-// Epilogue warp e's share (1/NW) of the block histogram is added to row `row`
-// of the global one and cleared, between two rounds on `bar` (NW arrivals a
-// round: every warp is done counting before anyone flushes, and done
-// flushing before anyone counts again).  False if the block gave up.
-template <int NW>
-__device__ __forceinline__ bool flush_hist(uint32_t *hist, uint32_t *ghist, int row, int e, int lane, uint64_t *bar,
-                                           uint32_t &bar_phase, volatile int *abort) {
+// One round on `bar` (one arrival per epilogue warp): every warp's shared-
+// memory reads and writes before it are visible to every warp after it.
+// False if the block gave up.
+__device__ __forceinline__ bool epi_round(int lane, uint64_t *bar, uint32_t &bar_phase, volatile int *abort) {
+  __syncwarp();
   int ok = 1;
   if (lane == 0) {
     mbar_arrive(bar);
     ok = mbar_wait_bounded(bar, bar_phase, abort) ? 1 : 0;
   }
   bar_phase ^= 1u;
-  if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
-  uint32_t *g = ghist + (size_t)row * kHistRowStride;
-  for (int i = e * (kHistBins / NW) + lane; i < (e + 1) * (kHistBins / NW); i += 32) {
-    const uint32_t c = hist[i];
-    if (c) {
-      atomicAdd(g + i, c);
-      hist[i] = 0;
-    }
-  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
-  if (lane == 0) {
-    mbar_arrive(bar);
-    ok = mbar_wait_bounded(bar, bar_phase, abort) ? 1 : 0;
+  return ok != 0;
+}
+
+// Adds the block's histogram to row `row` of the global ones and clears it;
+// epilogue warp e of NW takes every NW-th run of 32 bins.  Called between two
+// rounds (no warp counts meanwhile).
+template <int NW>
+__device__ __forceinline__ void flush_hist(uint32_t *hist, uint32_t *ghist, size_t row, int e, int lane) {
+  for (int i = e * 32 + lane; i < kHistBins; i += NW * 32) {
+    const uint32_t c = hist[i];
+    if (c == 0u) continue;
+    hist[i] = 0u;
+    atomicAdd(ghist + row * kHistRowStride + i, c);
   }
-  bar_phase ^= 1u;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // Largest visible position of a query group (-1 if none), clamped to [-1, T-1].
@@ -177,11 +190,12 @@ struct UnitCursor {
 
 // PGS: FP8 key scales in a paged pool (located through the block table);
 // a separate instantiation, so the contiguous FP8 epilogue pays nothing for it.
-template <int QG, bool F8 = false, bool PGS = false>
-__global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
+// HIST: p.ghist is non-null and receives the digit-0 histograms.
+template <int QG, bool F8 = false, bool PGS = false, bool HIST = false>
+__global__ void __launch_bounds__(Cfg<QG, F8, HIST>::kThreads, 1)
     indexer_scores_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                           const Params p) {
-  using C = Cfg<QG, F8>;
+  using C = Cfg<QG, F8, HIST>;
   constexpr int kPanelBytes = C::kPanelBytes;
   constexpr int kABytes = C::kABytes;
   constexpr int kUnitKeys = C::kUnitKeys;
@@ -200,10 +214,10 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
   uint64_t *hist_bar = mma_done + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(hist_bar + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  // [epilogue warps][queries per warp][64]: each epilogue warp keeps its own
-  // copy of its queries' head weights, so the warps never wait on one another.
-  float *sw_all = reinterpret_cast<float *>(small + 1024);
-  uint32_t *hist = reinterpret_cast<uint32_t *>(small + C::kSmall);  // QG == 1: [8192]
+  // one query: [epilogue warps][64], each warp's own copy of the head
+  // weights; several: [QG][64], the group's weights shared by the warps
+  float *sw_all = reinterpret_cast<float *>(small + 256);
+  uint32_t *hist = reinterpret_cast<uint32_t *>(small + C::kSmall);  // HIST: [8192]
   // FP8: [epilogue warps][kScaleDepth][32] key scales in flight
   float *scale_ring = reinterpret_cast<float *>(small + C::kSmall + C::kHistBytes);
 
@@ -234,8 +248,8 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
     prefetch_tensormap(&tmap_q);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
-  if (QG == 1 && p.ghist != nullptr)
-    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
+  if constexpr (HIST)
+    for (int i = threadIdx.x; i < C::kHistBytes / 4; i += blockDim.x) hist[i] = 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -379,8 +393,8 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
     const int sub = C::kSub > 1 ? (e >> 2) : 0;               // tile of the unit this warp reads
     const int qb = C::kSub > 1 ? 0 : (e >> 2) * QPW;          // first query (within the group) of this warp
     const int key_off = sub * kTileKeys + quarter * 32 + lane;  // this lane's key within a unit
-    float *sw = sw_all + e * QPW * kHeads;
-    const bool do_hist = QG == 1 && p.ghist != nullptr;
+    float *sw = C::kWarpWeights ? sw_all + e * QPW * kHeads : sw_all + qb * kHeads;
+    constexpr bool do_hist = HIST;
     uint32_t hist_phase = 0;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     int acc = 0;
@@ -424,19 +438,32 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
       const long long u = c.u, seg = c.seg;
       const int tile = c.tile;
       if (seg != cur_seg) {
-        if (do_hist && cur_seg >= 0 && !flush_hist<C::kEpiWarps>(hist, p.ghist, b, e, lane, hist_bar, hist_phase, abort_flag))
-          break;
+        // every warp is done with the previous group (its counts and, for
+        // several queries, the shared weights) before anyone flushes or
+        // reloads; for one query the rounds are needed only around a flush
+        const bool rounds = QG > 1 || (do_hist && cur_seg >= 0);
+        if (rounds && !epi_round(lane, hist_bar, hist_phase, abort_flag)) break;
+        if (do_hist && cur_seg >= 0) flush_hist<C::kEpiWarps>(hist, p.ghist, b, e, lane);
         b = c.b;
         q0 = c.g * QG;
         seg_max = group_max_pos<QG>(p, b, q0);
         __syncwarp();  // the warp is done with the previous group's weights
-        for (int i = lane; i < QPW * kHeads; i += 32) {
-          const int q = q0 + qb + i / kHeads;
+        // the warp's own copy, or the group's QG x 64 weights loaded by the
+        // warps between them
+        constexpr bool kWW = C::kWarpWeights;
+        const int w_first = kWW ? lane : e * 32 + lane;
+        const int w_step = kWW ? 32 : C::kEpiWarps * 32;
+        const int w_count = kWW ? QPW * kHeads : QG * kHeads;
+        const int w_q0 = kWW ? q0 + qb : q0;
+        float *w_dst = kWW ? sw : sw_all;
+        for (int i = w_first; i < w_count; i += w_step) {
+          const int q = w_q0 + i / kHeads;
           const size_t wi = ((size_t)b * p.Q + q) * kHeads + (i % kHeads);
           // FP8: the query head's scale folds into its weight (scales are
           // positive, so they pass through the ReLU)
-          sw[i] = q < p.Q ? __ldg(p.w + wi) * (F8 ? __ldg(p.q_scale + wi) : 1.0f) : 0.0f;
+          w_dst[i] = q < p.Q ? __ldg(p.w + wi) * (F8 ? __ldg(p.q_scale + wi) : 1.0f) : 0.0f;
         }
+        if (rounds && !epi_round(lane, hist_bar, hist_phase, abort_flag)) break;
 #pragma unroll
         for (int i = 0; i < QPW; ++i) {
           const int q = q0 + qb + i;
@@ -467,6 +494,12 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
         cp_async_wait<kSD - 1>();  // this unit's group has landed
         kscale = scale_ring[(e * kSD + ((u - u_begin) & (kSD - 1))) * 32 + lane];
       }
+      // each visible score's histogram bin, counted after the unit's
+      // scores are out (kNoBin: none)
+      constexpr uint32_t kNoBin = 0xFFFFFFFFu;
+      uint32_t hbin[QPW];
+#pragma unroll
+      for (int i = 0; i < QPW; ++i) hbin[i] = kNoBin;
 #pragma unroll
       for (int i = 0; i < QPW; ++i) {
         if (q0 + qb + i >= p.Q) break;
@@ -518,7 +551,13 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
           float *row = p.scores + ((size_t)b * p.Q + q0 + qb + i) * (size_t)p.T;
           const bool vis = real && key <= posv[i];
           row[key] = vis ? s : -INFINITY;
-          if (do_hist && vis) atomicAdd(&hist[score_key(s) >> kHistShift], 1u);
+          if constexpr (HIST) hbin[i] = vis ? score_key(s) >> kHistShift : kNoBin;
+        }
+      }
+      if constexpr (HIST) {
+#pragma unroll
+        for (int i = 0; i < QPW; ++i) {
+          if (hbin[i] != kNoBin) atomicAdd(&hist[hbin[i]], 1u);
         }
       }
       if (real) {
@@ -534,7 +573,8 @@ __global__ void __launch_bounds__(Cfg<QG, F8>::kThreads, 1)
       if constexpr (F8) prefetch_scale();
     }
     if constexpr (F8) asm volatile("cp.async.wait_all;" ::: "memory");
-    if (do_hist && cur_seg >= 0 && !*abort_flag) flush_hist<C::kEpiWarps>(hist, p.ghist, b, e, lane, hist_bar, hist_phase, abort_flag);
+    if (do_hist && cur_seg >= 0 && !*abort_flag && epi_round(lane, hist_bar, hist_phase, abort_flag))
+      flush_hist<C::kEpiWarps>(hist, p.ghist, b, e, lane);
   }
 
   tc_fence_before();

@@ -28,7 +28,15 @@
 // or a sort, so the result does not depend on thread scheduling.
 //
 // Two launch shapes:
-//   * many rows (prefill): one block per row does every step in shared memory;
+//   * many rows (prefill): one block per row does every step in shared
+//     memory.  A long row (at least 16 k scores) first plans from a sample:
+//     the digit-0 histogram of every 8th run of 32 scores gives a bin that,
+//     with a 4-sigma margin, has at least k scores at or above it; one pass
+//     then collects every score of that bin or above, in position order, and
+//     the exact k-th composite among them gives the selection.  So the row
+//     is read about 1.125 times.  Where the sample misjudged the row (fewer
+//     than k candidates, or more than the buffer holds), the exact steps
+//     below run as for any other row;
 //   * few long rows (decode): (chunk, row) blocks count step 1 (or it comes
 //     fused from the indexer); then, in one launch, (chunk, row) blocks each
 //     derive the row's plan (b0 and the rank of the k-th key within bin b0)
@@ -169,6 +177,35 @@ __device__ __forceinline__ uint32_t block_exclusive_sum(uint32_t v, uint32_t *to
   return before + x - v;
 }
 
+constexpr int kSampleStride = 8;    // one run of 32 scores in every 8 is sampled
+constexpr int kSampleMinRow = 16;   // rows of at least 16 k scores plan from the sample
+
+// Histogram of digit 0 over the sampled runs of [0, L): runs of 32 scores
+// (a 128-byte line each), every kSampleStride-th, warp w taking runs w,
+// w + 16, ...  Returns how many scores it counted.
+__device__ uint32_t hist_digit0_sampled(const float *srow, int L, uint32_t *hist) {
+  constexpr int kWarps = kThreads / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nsamp = ((L + 31) / 32 + kSampleStride - 1) / kSampleStride;
+  for (int r0 = warp; r0 < nsamp; r0 += kWarps * 4) {
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = r0 + u * kWarps;
+      const int i = r * (kSampleStride * 32) + lane;
+      v[u] = (r < nsamp && i < L) ? __ldg(srow + i) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = r0 + u * kWarps;
+      const int i = r * (kSampleStride * 32) + lane;
+      if (r < nsamp && i < L) atomicAdd(&hist[score_key(v[u]) >> kShift0], 1u);
+    }
+  }
+  const int last = (nsamp - 1) * kSampleStride * 32;  // first score of the last sampled run
+  return static_cast<uint32_t>((nsamp - 1) * 32 + min(32, L - last));
+}
+
 // Histogram of digit 0 of the row's keys over [start, end).
 __device__ void hist_digit0(const float *srow, int start, int end, uint32_t *hist) {
   for (int base = start; base < end; base += kThreads * kUnroll) {
@@ -269,7 +306,9 @@ __device__ __forceinline__ RowPlan plan_row_global(const uint32_t *g, uint32_t K
 // counted but not written.  PASS 1 chooses digit 0 > b0 (>= b0 with
 // take_b0) and, given hist1, counts digit 1 of bin b0 into it; PASS 2 chooses
 // bin b0 at sub-bin b1 or above.  Returns the count (the same in every thread).
-template <int PASS>
+// PREFETCH: the next iteration's scores are loaded before this iteration's
+// block-wide prefix sum (8 more registers a thread).
+template <int PASS, bool PREFETCH = true>
 __device__ uint32_t scan_ordered(const float *srow, int start, int end, const RowPlan &rp, uint32_t b1,
                                  uint32_t *hist1, uint64_t *dst, uint32_t cap, Scratch *sc) {
   uint32_t count = 0;
@@ -285,17 +324,30 @@ __device__ uint32_t scan_ordered(const float *srow, int start, int end, const Ro
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
   };
   const float thr = rp.take_b0 ? bin_floor(rp.b0) : (rp.b0 + 1 < static_cast<uint32_t>(kBins0) ? bin_floor(rp.b0 + 1) : kNever);
-  for (int base = start; base < end; base += kThreads * 8) {  // block-uniform trip count
-    const int i0 = base + threadIdx.x * 8;                   // 8 consecutive elements per thread
-    float val[8];
+  // 8 consecutive elements per thread
+  auto load8 = [&](int base, float (&v)[8]) {
+    const int i0 = base + threadIdx.x * 8;
     if (vec && i0 + 8 <= end) {
       const float4 a = __ldg(reinterpret_cast<const float4 *>(srow + i0));
       const float4 c = __ldg(reinterpret_cast<const float4 *>(srow + i0 + 4));
-      val[0] = a.x; val[1] = a.y; val[2] = a.z; val[3] = a.w;
-      val[4] = c.x; val[5] = c.y; val[6] = c.z; val[7] = c.w;
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
     } else {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) val[u] = i0 + u < end ? __ldg(srow + i0 + u) : kNever;
+      for (int u = 0; u < 8; ++u) v[u] = i0 + u < end ? __ldg(srow + i0 + u) : kNever;
+    }
+  };
+  float nxt[8];
+  if (PREFETCH && start < end) load8(start, nxt);
+  for (int base = start; base < end; base += kThreads * 8) {  // block-uniform trip count
+    const int i0 = base + threadIdx.x * 8;
+    float val[8];
+    if constexpr (PREFETCH) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) val[u] = nxt[u];
+      if (base + kThreads * 8 < end) load8(base + kThreads * 8, nxt);
+    } else {
+      load8(base, val);
     }
     uint32_t takes = 0;
     if (PASS == 1) {
@@ -498,6 +550,34 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const float *__restr
   const float *srow = scores + (size_t)row * T;
   int32_t *out = idx + (size_t)row * K;
   if (write_short_row(L, K, out)) return;
+  if (L >= kSampleMinRow * K) {
+    // the plan from a sample: the bin with m sampled scores at or above it,
+    // m = e + 4 sqrt(e) + 1 for e = k x (sampled / L) the sample's share of
+    // the k winners
+    for (int i = threadIdx.x; i < kBins0; i += kThreads) s.hist[i] = 0;
+    __syncthreads();
+    const uint32_t ns = hist_digit0_sampled(srow, L, s.hist);
+    __syncthreads();
+    const float e = static_cast<float>(K) * static_cast<float>(ns) / static_cast<float>(L);
+    const uint32_t m = static_cast<uint32_t>(ceilf(e + 4.0f * sqrtf(e))) + 1u;
+    if (m <= ns) {
+      find_threshold_bin<kBins0>(s.hist, m, &sc);
+      RowPlan rp;
+      rp.b0 = sc.result[0];
+      rp.need1 = 0;
+      rp.take_b0 = true;
+      __syncthreads();
+      const uint32_t n = scan_ordered<1>(srow, 0, L, rp, 0, nullptr, s.cand, kSmemCand, &sc);
+      __syncthreads();
+      if (n >= static_cast<uint32_t>(K) && n <= static_cast<uint32_t>(kSmemCand)) {
+        // every score outside the candidates is below every candidate
+        const uint64_t tau = select_threshold(s.cand, n, static_cast<uint32_t>(K), s.hist, &sc);
+        write_ordered(s.cand, n, tau, K, out, &sc);
+        return;
+      }
+      // the sample misjudged the row: the exact steps
+    }
+  }
   uint32_t *hist1 = reinterpret_cast<uint32_t *>(s.sortbuf);  // the sort buffer is free until the end
   for (int i = threadIdx.x; i < kBins0; i += kThreads) s.hist[i] = 0;
   for (int i = threadIdx.x; i < kBins; i += kThreads) hist1[i] = 0;
@@ -523,8 +603,8 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const float *__restr
 }
 
 // --------------------------------------------------------------------------
-// Few long rows: (chunk, row) blocks.  ghist [rows][kGhistStride] (digit 0 in
-// the first kBins0 words) and done [rows] must be zero before step 1 (one
+// Few long rows: (chunk, row) blocks.  ghist [rows][kGhistStride] (the
+// digit-0 histograms) and done [rows] must be zero before step 1 (one
 // memset clears both).  cand [rows][T] holds each chunk's candidates at the
 // chunk's own offset; counts [rows][nchunk] how many each chunk left.
 // --------------------------------------------------------------------------
@@ -539,7 +619,7 @@ struct ChunkParams {
   int32_t *idx;
 };
 
-constexpr int kGhistStride = kBins0 + kBins;  // per-row words of ghist
+constexpr int kGhistStride = kBins0;  // per-row words of ghist
 // The row's last block copies up to this many candidates into its dynamic
 // shared memory (40 KB: four 512-thread blocks of the scan still fit an SM)
 // and selects there; a row with more reads them in place from L2.
@@ -668,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 4) topk_chunk_scan_select_kernel(con
   rp.take_b0 = true;
   const uint64_t *crow = p.cand + (size_t)row * p.T;
   // never exceeded: positions are distinct
-  const uint32_t n = scan_ordered<1>(p.scores + (size_t)row * p.T, start, end, rp, 0, nullptr,
+  const uint32_t n = scan_ordered<1, false>(p.scores + (size_t)row * p.T, start, end, rp, 0, nullptr,
                                      p.cand + (size_t)row * p.T + start, static_cast<uint32_t>(end - start), &sc);
   if (threadIdx.x == 0) p.counts[(size_t)row * p.nchunk + c] = n;
   // the kernel after this one (the attention, a dependent launch) may start

@@ -102,13 +102,26 @@ def _topk_case(scores_np, pos_np, k):
     (1, 320, 5000, 2048, "normal"),      # many rows: one block per row
     (1, 320, 3000, 700, "ints"),
     (1, 300, 13000, 2048, "equal"),      # many rows, candidates overflow shared memory: fallback passes
+    (1, 300, 40_000, 2048, "normal"),    # long rows: the plan from a sample, one pass
+    (1, 300, 40_000, 2048, "unsampled"), # the winners mostly outside the sampled runs
+    (1, 300, 40_000, 2048, "sampled"),   # the winners only inside the sampled runs: the sample misjudges, exact steps
+    (1, 296, 33_000, 2048, "equal"),     # long rows of one value: too many candidates, exact steps
+    (1, 300, 12_000, 700, "ints"),       # long rows for a small k, heavy ties
     (4, 1, 9000, 7, "normal"),           # tiny k
     (2, 2, 1500, 2048, "normal"),        # L < k: -1 padding
 ])
 def test_topk_bit_exact(B, Q, T, k, kind):
     rng = np.random.default_rng(T + k)
-    if kind == "normal":
+    if kind in ("normal", "unsampled", "sampled"):
         s = rng.standard_normal((B, Q, T))
+        # one run of 32 scores in every 8 is sampled by the long-row plan
+        in_sample = (np.arange(T) // 32) % 8 == 0
+        if kind == "unsampled":
+            boost = ~in_sample & (rng.random(T) < 0.05)
+            s[..., boost] += 6.0
+        elif kind == "sampled":
+            boost = in_sample & (rng.random(T) < 0.4)
+            s[..., boost] += 6.0
     elif kind == "ints":
         s = rng.integers(0, 50, (B, Q, T)).astype(np.float64)
     else:
@@ -307,6 +320,14 @@ def test_group_equals_four_independent_layers():
     assert torch.equal(idx, idx2)
 
 
+def _digit0_hist(scores_row: np.ndarray, L: int) -> np.ndarray:
+    """Counts of the top 13 bits of the order-preserving key of each fp32 score
+    (sign folded, -0 as +0) over positions [0, L): the top-k's first digit."""
+    bits = (scores_row[:L].astype(np.float32) + np.float32(0.0)).view(np.uint32)
+    key = np.where(bits & np.uint32(0x80000000), ~bits, bits | np.uint32(0x80000000))
+    return np.bincount((key >> np.uint32(19)).astype(np.int64), minlength=8192)
+
+
 @pytest.mark.parametrize("B,T,dup", [(3, 50_000, False), (2, 120_000, True), (5, 9_000, True)])
 def test_group_decode_topk_bit_exact(B, T, dup):
     """One query per sequence over a long context: the group's index set (whose
@@ -322,12 +343,52 @@ def test_group_decode_topk_bit_exact(B, T, dup):
     kv = [wl.latent_cache(B, T, 5, layer, DEV) for layer in range(4)]
     outs = [torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=DEV) for _ in range(4)]
     idx = torch.empty(B, 1, 2048, dtype=torch.int32, device=DEV)
-    dsa.indexshare_group_forward(cfg, q_idx, w, k_idx, pos, q, kv, outs, idx, dsa.alloc_workspace(cfg, B, 1, T, 4))
+    ws = dsa.alloc_workspace(cfg, B, 1, T, 4)
+    dsa.indexshare_group_forward(cfg, q_idx, w, k_idx, pos, q, kv, outs, idx, ws)
     scores = torch.empty(B, 1, T, device=DEV)
     dsa.indexer_scores(cfg, q_idx, w, k_idx, pos, scores)
     torch.cuda.synchronize()
     ora = oracle.topk_select(scores.cpu().double().numpy(), pos.cpu().numpy(), 2048)
     assert np.array_equal(idx.cpu().numpy(), ora)
+    # the histogram the indexer counted (it follows the scores in the
+    # workspace, 256-byte aligned) is a count over each row's visible scores
+    off = -(-B * T * 4 // 256) * 256
+    hist = ws[off:off + B * 8192 * 4].view(torch.int32).view(B, 8192).cpu().numpy()
+    g = _workspace_scores(ws, B, 1, T).cpu().numpy()
+    for b in range(B):
+        assert np.array_equal(hist[b], _digit0_hist(g[b, 0], int(pos[b, 0]) + 1)), b
+
+
+@pytest.mark.parametrize("B,Q,T,keys", [
+    (1, 4, 70_000, "equal"),     # four queries per group, every score of a row equal
+    (2, 2, 50_000, "dup"),       # two queries per group
+    (3, 7, 40_000, "dup"),       # ragged last group of four
+    (1, 300, 40_000, "dup"),     # one block per row, the plan from a sample
+    (1, 296, 70_000, "equal"),   # one block per row, one value: exact steps
+])
+def test_group_multi_query_topk_bit_exact(B, Q, T, keys):
+    """Several queries per sequence: the group's index set equals the oracle's
+    top-k of the very same fp32 scores, bit for bit."""
+    cfg = dsa.default_config()
+    q_idx, w, k_idx, pos = _indexer_inputs(B, Q, T, T - Q, seed=T + Q)
+    if keys == "equal":     # every key the same: every visible score of a row in one bin
+        k_idx[:] = k_idx[:, :1].clone()
+    else:                   # identical scores at different positions
+        k_idx[:, T // 2:T // 2 + 3000] = k_idx[:, 1000:4000]
+        k_idx[:, T - 500:] = k_idx[:, 200:700]
+    q = [wl.mla_queries(B, Q, 5, layer, DEV) for layer in range(4)]
+    kv = [wl.latent_cache(B, T, 5, layer, DEV) for layer in range(4)]
+    outs = [torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV) for _ in range(4)]
+    idx = torch.empty(B, Q, 2048, dtype=torch.int32, device=DEV)
+    ws = dsa.alloc_workspace(cfg, B, Q, T, 4)
+    dsa.indexshare_group_forward(cfg, q_idx, w, k_idx, pos, q, kv, outs, idx, ws)
+    torch.cuda.synchronize()
+    g_scores = _workspace_scores(ws, B, Q, T).cpu().numpy()
+    P = pos.cpu().numpy()
+    ora = oracle.topk_select(g_scores.astype(np.float64), P, 2048)
+    assert np.array_equal(idx.cpu().numpy(), ora)
+    if keys == "equal":
+        assert np.array_equal(ora[..., :2048], np.broadcast_to(np.arange(2048), ora.shape))
 
 
 def test_group_is_deterministic():
