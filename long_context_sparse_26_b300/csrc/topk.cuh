@@ -182,21 +182,23 @@ constexpr int kSampleMinRow = 16;   // rows of at least 16 k scores plan from th
 
 // Histogram of digit 0 over the sampled runs of [0, L): runs of 32 scores
 // (a 128-byte line each), every kSampleStride-th, warp w taking runs w,
-// w + 16, ...  Returns how many scores it counted.
+// w + 16, ..., eight loads a lane in flight.  Returns how many scores it
+// counted.
 __device__ uint32_t hist_digit0_sampled(const float *srow, int L, uint32_t *hist) {
   constexpr int kWarps = kThreads / 32;
+  constexpr int kU = 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nsamp = ((L + 31) / 32 + kSampleStride - 1) / kSampleStride;
-  for (int r0 = warp; r0 < nsamp; r0 += kWarps * 4) {
-    float v[4];
+  for (int r0 = warp; r0 < nsamp; r0 += kWarps * kU) {
+    float v[kU];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kU; ++u) {
       const int r = r0 + u * kWarps;
       const int i = r * (kSampleStride * 32) + lane;
       v[u] = (r < nsamp && i < L) ? __ldg(srow + i) : 0.0f;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kU; ++u) {
       const int r = r0 + u * kWarps;
       const int i = r * (kSampleStride * 32) + lane;
       if (r < nsamp && i < L) atomicAdd(&hist[score_key(v[u]) >> kShift0], 1u);
@@ -539,7 +541,7 @@ __device__ void finish_row(const uint64_t *cand, uint32_t n, int K, const RowPla
 // --------------------------------------------------------------------------
 // Many rows: one block per row does every step in shared memory.
 // --------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) topk_row_kernel(const float *__restrict__ scores,
+__global__ void __launch_bounds__(kThreads, 2) topk_row_kernel(const float *__restrict__ scores,
                                                             const int32_t *__restrict__ q_pos, int T, int K,
                                                             int32_t *__restrict__ idx) {
   extern __shared__ __align__(16) uint8_t smem[];
