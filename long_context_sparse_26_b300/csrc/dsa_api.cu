@@ -412,7 +412,8 @@ dsa_status_t enqueue_attention(const dsa::attn::Params &p, int B, cudaStream_t s
   // a programmatic dependent launch: the blocks may start (barriers, tensor
   // memory, the query panels) while the kernel before them on the stream
   // finishes; they wait for it (griddepcontrol.wait) before reading idx
-  const dim3 grid(static_cast<unsigned>(blocks)), block(dsa::mla::kThreads);
+  const dim3 grid(static_cast<unsigned>(blocks));
+  const dim3 block(p.kv_fp8 ? dsa::mla::Roles<true>::kThreads : dsa::mla::Roles<false>::kThreads);
   const cudaError_t e =
       p.kv_fp8 ? launch_dependent(dsa::mla::sparse_mla_tc_kernel<true>, grid, block, dsa::mla::kSmemBytes, stream, maps, p)
                : launch_dependent(dsa::mla::sparse_mla_tc_kernel<false>, grid, block, dsa::mla::kSmemBytes, stream, maps,

@@ -36,9 +36,9 @@
 // running sum before that window's GEMM 2.  Anything in between stays within
 // fp32 range, and the final O / l is the same for every choice of reference.
 //
-// Warp roles (kThreads threads, one block per SM):
-//   producers  5 warps: rows w, w + 5, ... of every window; warp 0 also loads
-//              the query panels by TMA;
+// Warp roles (one block per SM):
+//   producers  9 warps (bf16 rows) or 5 (FP8 rows): rows w, w + P, ... of
+//              every window; warp 0 also loads the query panels by TMA;
 //   GEMM 1     two warps, one issuing thread each, on alternate panel groups
 //              into two partial S tiles (the first also allocates tensor
 //              memory); GEMM 2 a third: one thread issues these small MMAs at
@@ -76,15 +76,25 @@ constexpr int kGroups = 5;                           // panel groups of a window
 constexpr int kPanelBytes = kRingRows * 128;         // one 64-dim panel of the ring: 16 KB
 constexpr int kRingBytes = kPanels * kPanelBytes;    // 147456
 constexpr int kQBytes = kPanels * kH * 128;          // 73728
-constexpr int kProducerWarps = 5;
-constexpr int kMmaWarp = kProducerWarps;             // tensor-memory allocation, GEMM 1 on groups 0, 2, 4
-constexpr int kMma1bWarp = kProducerWarps + 1;       // GEMM 1 on groups 1, 3
-constexpr int kGemm2Warp = kProducerWarps + 2;       // GEMM 2 issue
-constexpr int kSoftmaxWarp0 = kProducerWarps + 3;    // four softmax warps, one per TMEM lane quarter
-constexpr int kThreads = 32 * (kProducerWarps + 3 + 4);
-constexpr int kRowsPerWarp = (kKeys + kProducerWarps - 1) / kProducerWarps;  // rows of a window per producer warp
-constexpr int kPatA = (kRowsPerWarp + 1) / 2;        // copy instructions of a two-panel group (two rows each)
-constexpr int kPatB = (kRowsPerWarp + 3) / 4;        // copy instructions of the RoPE panel (four rows each)
+// Warp roles: the producers, then the three MMA-issuing warps, then four
+// softmax warps.  bf16 rows: nine producer warps (random 1152-byte rows are
+// gathered faster the more warps issue the copies: 2.9 TB/s from five warps,
+// 4.6 TB/s from nine, measured on a B300); FP8 rows: five (their
+// dequantisation needs the registers of a 384-thread block).
+template <bool F8KV>
+struct Roles {
+  static constexpr int kProducerWarps = F8KV ? 5 : 9;
+  static constexpr int kMmaWarp = kProducerWarps;           // tensor-memory allocation, GEMM 1 on groups 0, 2, 4
+  static constexpr int kMma1bWarp = kProducerWarps + 1;     // GEMM 1 on groups 1, 3
+  static constexpr int kGemm2Warp = kProducerWarps + 2;     // GEMM 2 issue
+  static constexpr int kSoftmaxWarp0 = kProducerWarps + 3;  // four softmax warps, one per TMEM lane quarter
+  static constexpr int kThreads = 32 * (kProducerWarps + 3 + 4);
+  static constexpr int kRowsPerWarp = (kKeys + kProducerWarps - 1) / kProducerWarps;  // rows of a window per producer warp
+  static constexpr int kPatA = (kRowsPerWarp + 1) / 2;      // copy instructions of a two-panel group (two rows each)
+  static constexpr int kPatB = (kRowsPerWarp + 3) / 4;      // copy instructions of the RoPE panel (four rows each)
+  static_assert(kSoftmaxWarp0 % 4 == 0, "softmax warp w reads TMEM lane quarter w % 4");
+};
+constexpr int kMaxProducerWarps = 9;
 // FP8 latent rows are gathered and converted in stages of 32 rows, two per window
 constexpr int kStageRows = 32;
 constexpr int kStages = kRingRows / kStageRows;      // 4
@@ -94,10 +104,9 @@ constexpr int kTmemCols = 512;
 constexpr int kOCol = 0;
 constexpr int kSCol = 256;                           // S partial of groups 0, 2, 4; two window buffers
 constexpr int kSColB = 384;                          // S partial of groups 1, 3; two window buffers
-constexpr int kSmallBytes = 1024;
+constexpr int kSmallBytes = 2048;
 constexpr int kSmemBytes = 1024 + kQBytes + kRingBytes + kSmallBytes;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
-static_assert(kSoftmaxWarp0 % 4 == 0, "softmax warp w reads TMEM lane quarter w % 4");
 static_assert(kRingBytes >= kH * kDv * 4, "the epilogue stages an fp32 partial in the gather ring");
 static_assert(kKeys % kStageRows == 0 && kKeys % 32 == 0 && kKeys == 64, "windows of 64 keys");
 static_assert(kSColB + 2 * kKeys <= kTmemCols && kSCol + 2 * kKeys <= kSColB, "S partials fit the allocation");
@@ -222,7 +231,7 @@ struct Small {
   uint64_t mma_done;
   uint64_t mma1b_done;
   uint64_t mma2_done;
-  uint64_t staged[kProducerWarps][kStages];  // FP8 latent rows: a warp's copies of a stage have landed
+  uint64_t staged[kMaxProducerWarps][kStages];  // FP8 latent rows: a warp's copies of a stage have landed
   uint32_t tmem_slot;
   int abort;
   int status[2][4];               // per softmax warp, per window parity: 1 = ok
@@ -246,8 +255,12 @@ __device__ __forceinline__ void dequant16(const uint4 &code, float scale, uint32
 }
 
 template <bool F8KV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<F8KV>::kThreads, 1)
     sparse_mla_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
+  using R = Roles<F8KV>;
+  constexpr int kProducerWarps = R::kProducerWarps, kMmaWarp = R::kMmaWarp, kMma1bWarp = R::kMma1bWarp;
+  constexpr int kGemm2Warp = R::kGemm2Warp, kSoftmaxWarp0 = R::kSoftmaxWarp0;
+  constexpr int kRowsPerWarp = R::kRowsPerWarp, kPatA = R::kPatA, kPatB = R::kPatB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sQ = base;                                  // [9 panels][64 heads][128 B]
