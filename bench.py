@@ -771,6 +771,9 @@ def profile_kernel(args, w: wl.Workload):
             dsa.indexer_scores(cfg, q_idx, wt, k_idx, q_pos, scores)
         elif kind == "topk":
             dsa.topk_select(cfg, scores, q_pos, idx, ws)
+        elif kind == "attention" and not args.fp8_kv and w.kind != "mtp":
+            # every layer in one launch over the shared index set, as the group makes it
+            dsa.sparse_mla_attn_shared(cfg, q, kv, idx, outs, ws)
         elif kind == "attention":
             for layer in range(n_att):
                 attn = dsa.sparse_mla_attn_fp8 if args.fp8_kv else dsa.sparse_mla_attn

@@ -808,16 +808,30 @@ __global__ void __launch_bounds__(Roles<F8KV>::kThreads, 1)
         pm[head * 2 + 1] = ok ? l : 0.0f;
       }
     }
-    const int tid = threadIdx.x - 32 * kSoftmaxWarp0;  // 0..127
+  }
+
+  // ---- the block's result, stored by every warp: once the softmax warps
+  // have published 1/l and the block's status (and, when it is ok, the last
+  // GEMM 2 has completed), warp w takes the 128-dim chunks w / 4, w / 4 +
+  // (warps / 4), ... of O^T for its TMEM lane quarter w % 4, straight from
+  // tensor memory to global memory: lane = dim, so for each head a warp's
+  // stores cover 32 consecutive dims (coalesced).  After an abort the
+  // tensor memory is not read (an MMA may still be writing it): zeros.
+  tc_fence_before();
+  __syncthreads();
+  {
+    const bool ok = sm->status[0][0] && sm->status[0][1] && sm->status[0][2] && sm->status[0][3];
+    const size_t rowL = (size_t)layer * p.rows + row;
+    const bool one = p.nsplit == 1;
     if (ok && nblk > 0) {
-      // straight from tensor memory to global memory: lane = dim, so for each
-      // head a warp's stores cover 32 consecutive dims (coalesced)
       tc_fence_after();
+      const float *inv_l = sm->xa[0];
+      const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
       float *po = one ? nullptr : p.part_o + ((rowL * p.nsplit + split) * kH) * kDv;
       __nv_bfloat16 *bo = one ? p.out[layer] + (size_t)row * kH * kDv : nullptr;
 #pragma unroll 1
-      for (int c = 0; c < kDv / 128; ++c) {
-        const int d = c * 128 + q4 * 32 + lane;
+      for (int c = warp >> 2; c < kDv / 128; c += R::kThreads / 128) {
+        const int d = c * 128 + (warp & 3) * 32 + lane;
         uint32_t r0[32], r1[32];
         tmem_ld_32x32b_x32_nowait(tmem_base + lane_addr + kOCol + c * 64, r0);
         tmem_ld_32x32b_x32_nowait(tmem_base + lane_addr + kOCol + c * 64 + 32, r1);
@@ -837,11 +851,10 @@ __global__ void __launch_bounds__(Roles<F8KV>::kThreads, 1)
         }
       }
     } else {
-      // no index in this slice, or the block gave up: zeros
       uint4 *dst = one ? reinterpret_cast<uint4 *>(p.out[layer] + (size_t)row * kH * kDv)
                        : reinterpret_cast<uint4 *>(p.part_o + ((rowL * p.nsplit + split) * kH) * kDv);
       const int n16 = one ? kH * kDv * 2 / 16 : kH * kDv * 4 / 16;
-      for (int i = tid; i < n16; i += 128) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      for (int i = threadIdx.x; i < n16; i += R::kThreads) dst[i] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
 
