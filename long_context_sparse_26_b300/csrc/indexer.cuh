@@ -494,12 +494,6 @@ __global__ void __launch_bounds__(Cfg<QG, F8, HIST>::kThreads, 1)
         cp_async_wait<kSD - 1>();  // this unit's group has landed
         kscale = scale_ring[(e * kSD + ((u - u_begin) & (kSD - 1))) * 32 + lane];
       }
-      // each visible score's histogram bin, counted after the unit's
-      // scores are out (kNoBin: none)
-      constexpr uint32_t kNoBin = 0xFFFFFFFFu;
-      uint32_t hbin[QPW];
-#pragma unroll
-      for (int i = 0; i < QPW; ++i) hbin[i] = kNoBin;
 #pragma unroll
       for (int i = 0; i < QPW; ++i) {
         if (q0 + qb + i >= p.Q) break;
@@ -551,13 +545,9 @@ __global__ void __launch_bounds__(Cfg<QG, F8, HIST>::kThreads, 1)
           float *row = p.scores + ((size_t)b * p.Q + q0 + qb + i) * (size_t)p.T;
           const bool vis = real && key <= posv[i];
           row[key] = vis ? s : -INFINITY;
-          if constexpr (HIST) hbin[i] = vis ? score_key(s) >> kHistShift : kNoBin;
-        }
-      }
-      if constexpr (HIST) {
-#pragma unroll
-        for (int i = 0; i < QPW; ++i) {
-          if (hbin[i] != kNoBin) atomicAdd(&hist[hbin[i]], 1u);
+          // (measured: this inline count beats one deferred past the store)
+          if constexpr (HIST)
+            if (vis) atomicAdd(&hist[score_key(s) >> kHistShift], 1u);
         }
       }
       if (real) {
