@@ -737,7 +737,11 @@ def profile_kernel(args, w: wl.Workload):
     dev = "cuda"
     cfg = dsa.default_config(topk=w.topk)
     B, Q, T = w.B, w.Q, w.T
-    q_pos = torch.arange(w.first_pos, w.first_pos + Q, dtype=torch.int32, device=dev).repeat(B, 1).contiguous()
+    first = w.first_pos
+    if args.queries and args.queries < Q:  # the last query tokens of the workload only (a smaller capture)
+        first += Q - args.queries
+        Q = args.queries
+    q_pos = torch.arange(first, first + Q, dtype=torch.int32, device=dev).repeat(B, 1).contiguous()
     n_att = w.mtp_steps if w.kind == "mtp" else w.n_layers
     ws = dsa.alloc_workspace(cfg, B, Q, T, n_att, dev)
     scores = torch.empty(B, Q, T, device=dev)
@@ -782,7 +786,7 @@ def profile_kernel(args, w: wl.Workload):
             dsa.indexshare_group_forward(cfg, q_idx, wt, k_idx, q_pos, q, kv, outs, idx, ws)
     torch.cuda.synchronize()
     status = dsa.get_device_error()
-    print(json.dumps({"profile_kernel": kind, "workload": w.name, "B": B, "Q": Q, "T": T,
+    print(json.dumps({"profile_kernel": kind, "workload": w.name, "B": B, "Q": Q, "first_pos": first, "T": T,
                       "launches": args.warmup + args.steps, "device_error": status}))
     if status != 0:
         sys.exit(1)
@@ -816,6 +820,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-read-peak", action="store_true", help="skip the read-only stream measurement")
     ap.add_argument("--batch", type=int, default=None, help="smaller batch (a small case for profiling)")
+    ap.add_argument("--queries", type=int, default=None,
+                    help="with --profile-kernel: only the workload's last N query tokens (a small case)")
     ap.add_argument("--fp8-indexer", action="store_true",
                     help="store the indexer caches as FP8 (E4M3) rows with fp32 scales (decode workloads)")
     ap.add_argument("--fp8-kv", action="store_true",

@@ -328,17 +328,26 @@ def _digit0_hist(scores_row: np.ndarray, L: int) -> np.ndarray:
     return np.bincount((key >> np.uint32(19)).astype(np.int64), minlength=8192)
 
 
-@pytest.mark.parametrize("B,T,dup", [(3, 50_000, False), (2, 120_000, True), (5, 9_000, True)])
-def test_group_decode_topk_bit_exact(B, T, dup):
+@pytest.mark.parametrize("B,T,pattern", [
+    (3, 50_000, "none"),
+    (2, 120_000, "dup"),     # exact ties made by duplicated keys
+    (5, 9_000, "dup"),
+    (2, 120_000, "hot"),     # a few scaled-up keys dominate the row
+    (3, 9_000, "short"),     # rows barely longer than k among long ones
+])
+def test_group_decode_topk_bit_exact(B, T, pattern):
     """One query per sequence over a long context: the group's index set (whose
     first histogram is counted inside the indexer) equals the oracle's top-k of
-    the very same fp32 scores, bit for bit, including exact ties made by
-    duplicated keys."""
+    the very same fp32 scores, bit for bit."""
     cfg = dsa.default_config()
     q_idx, w, k_idx, pos = _indexer_inputs(B, 1, T, T - 1, seed=T + B)
-    if dup:   # copy a block of keys elsewhere: identical scores at different positions
+    if pattern == "dup":   # copy a block of keys elsewhere: identical scores at different positions
         k_idx[:, T // 2:T // 2 + 3000] = k_idx[:, 1000:4000]
         k_idx[:, T - 500:] = k_idx[:, 200:700]
+    elif pattern == "hot":   # every 50th key scaled up 4x: their scores dominate
+        k_idx[:, ::50] *= 4
+    elif pattern == "short":
+        pos[:, 0] = torch.tensor([T - 1, 2099, 2500], dtype=torch.int32, device=DEV)[:B]
     q = [wl.mla_queries(B, 1, 5, layer, DEV) for layer in range(4)]
     kv = [wl.latent_cache(B, T, 5, layer, DEV) for layer in range(4)]
     outs = [torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=DEV) for _ in range(4)]
