@@ -237,11 +237,25 @@ TopkShape topk_shape(int rows, int T, int sms) {
 
 struct AttnShape {
   int nsplit = 1, bps = 1;
+  // one split per (layer, row) unit, except that the units from tail_base
+  // on (the last, partial wave) take tail_nsplit splits of tail_bps windows
+  long long tail_base = 0;
+  int tail_nsplit = 0, tail_bps = 0;
+  long long blocks(long long rowsL) const {
+    return tail_nsplit > 0 ? tail_base + (rowsL - tail_base) * tail_nsplit : rowsL * nsplit;
+  }
+  // (layer, row) units whose splits leave fp32 partials, and splits each
+  long long partial_units(long long rowsL) const { return tail_nsplit > 0 ? rowsL - tail_base : (nsplit > 1 ? rowsL : 0); }
+  int partial_splits() const { return tail_nsplit > 0 ? tail_nsplit : nsplit; }
 };
 
+constexpr int kSplitCost = 7;  // windows' worth of a split's partial (written, then read by the combine)
+
 // Splits of each row's index slots over blocks (one block per SM at a time):
-// the fewest waves x tiles per block, where a split also costs its fp32
-// partial (written, then read by the combine: about 7 tiles' worth of bytes).
+// the fewest waves x windows per block, where a split also costs its fp32
+// partial.  With one split per unit, the units of a last, partial wave are
+// split further when that shortens it, so that wave runs as wide as the GPU
+// (wave quantisation: 512 units on 148 SMs leave a fourth wave 46% full).
 AttnShape attn_shape(long long rowsL, int K, int sms) {
   AttnShape best;
   const int nblocks = (K + dsa::mla::kKeys - 1) / dsa::mla::kKeys;
@@ -250,11 +264,26 @@ AttnShape attn_shape(long long rowsL, int K, int sms) {
     const int bps = (nblocks + ns - 1) / ns;
     const int nsr = (nblocks + bps - 1) / bps;
     const long long waves = (rowsL * nsr + sms - 1) / sms;
-    const long long cost = waves * (bps + (nsr > 1 ? 7 : 0));
+    const long long cost = waves * (bps + (nsr > 1 ? kSplitCost : 0));
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best.nsplit = nsr;
       best.bps = bps;
+    }
+  }
+  if (best.nsplit == 1) {
+    const long long full = rowsL / sms * sms;
+    const long long rem = rowsL - full;
+    if (full > 0 && rem > 0) {
+      long long s = sms / rem;
+      s = s < 16 ? s : 16;
+      s = s < nblocks ? s : nblocks;
+      const int bps = static_cast<int>((nblocks + s - 1) / s);
+      if (s >= 2 && bps + kSplitCost < nblocks) {
+        best.tail_base = full;
+        best.tail_bps = bps;
+        best.tail_nsplit = (nblocks + bps - 1) / bps;
+      }
     }
   }
   return best;
@@ -267,12 +296,9 @@ struct Layout {
 
 size_t attn_partial_bytes(long long rowsL, int K, int sms, size_t *ml_bytes) {
   const AttnShape a = attn_shape(rowsL, K, sms);
-  if (a.nsplit <= 1) {
-    *ml_bytes = 0;
-    return 0;
-  }
-  *ml_bytes = static_cast<size_t>(rowsL) * a.nsplit * kHeads * 2 * sizeof(float);
-  return static_cast<size_t>(rowsL) * a.nsplit * kHeads * kLora * sizeof(float);
+  const size_t tiles = static_cast<size_t>(a.partial_units(rowsL)) * a.partial_splits();
+  *ml_bytes = tiles * kHeads * 2 * sizeof(float);
+  return tiles * kHeads * kLora * sizeof(float);
 }
 
 Layout layout(int B, int Q, int T, int n_layers, int K, int sms) {
@@ -408,7 +434,8 @@ dsa_status_t enqueue_attention(const dsa::attn::Params &p, int B, cudaStream_t s
   for (int l = 0; l < p.n_layers; ++l)
     if (!make_tmap_576(&maps.q[l], p.q[l], static_cast<unsigned long long>(p.rows) * kHeads, kHeads))
       return DSA_ERR_CUDA;
-  const long long blocks = static_cast<long long>(p.n_layers) * p.nsplit * p.rows;
+  const long long rowsL = static_cast<long long>(p.n_layers) * p.rows;
+  const long long blocks = p.tail_nsplit > 0 ? p.tail_base + (rowsL - p.tail_base) * p.tail_nsplit : rowsL * p.nsplit;
   // a programmatic dependent launch: the blocks may start (barriers, tensor
   // memory, the query panels) while the kernel before them on the stream
   // finishes; they wait for it (griddepcontrol.wait) before reading idx
@@ -419,8 +446,9 @@ dsa_status_t enqueue_attention(const dsa::attn::Params &p, int B, cudaStream_t s
                : launch_dependent(dsa::mla::sparse_mla_tc_kernel<false>, grid, block, dsa::mla::kSmemBytes, stream, maps,
                                   p);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
-  if (p.nsplit > 1) {
-    const dim3 cgrid(kHeads, static_cast<unsigned>(static_cast<long long>(p.rows) * p.n_layers));
+  if (p.nsplit > 1 || p.tail_nsplit > 0) {
+    const long long cunits = p.tail_nsplit > 0 ? rowsL - p.tail_base : rowsL;
+    const dim3 cgrid(kHeads, static_cast<unsigned>(cunits));
     if (launch_dependent(dsa::attn::combine_kernel, cgrid, dim3(128), 0, stream, p) != cudaSuccess)
       return DSA_ERR_CUDA;
   }
@@ -453,6 +481,9 @@ dsa_status_t launch_attention(const DeviceState &dev, const Layout &L, uint8_t *
   const AttnShape a = attn_shape(static_cast<long long>(rows) * n_layers, K, dev.sms);
   p.nsplit = a.nsplit;
   p.blocks_per_split = a.bps;
+  p.tail_base = static_cast<int>(a.tail_base);
+  p.tail_nsplit = a.tail_nsplit;
+  p.tail_bps = a.tail_bps;
   p.part_o = reinterpret_cast<float *>(ws + L.part_o);
   p.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
   p.scale_log2 = sm_scale * 1.4426950408889634f;

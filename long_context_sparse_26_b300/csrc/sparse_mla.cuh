@@ -37,8 +37,12 @@ struct Params {
   int n_layers, Q, T, K;
   int rows;                             // B*Q
   int nsplit, blocks_per_split;
-  float *part_o;                        // [n_layers*rows, nsplit, 64, 512]
-  float *part_ml;                       // [n_layers*rows, nsplit, 64, 2]
+  // units (layer u % n_layers, row u / n_layers) from tail_base on take
+  // tail_nsplit splits of tail_bps windows instead (tail_nsplit 0: none;
+  // then nsplit is 1); their partials are tiles (u - tail_base) * tail_nsplit + split
+  int tail_base, tail_nsplit, tail_bps;
+  float *part_o;                        // [n_layers*rows, nsplit, 64, 512], or the tail units' tiles
+  float *part_ml;                       // [n_layers*rows, nsplit, 64, 2], likewise
   float scale_log2;                     // sm_scale * log2(e)
   // paged latent caches (block_table null: kv[l] is [B, T, 576] contiguous):
   // position s of sequence b is row block_table[b][s / page_size] * page_size
@@ -50,26 +54,39 @@ struct Params {
 
 // Merges the splits of one (layer, row, head): O = sum_s 2^(m_s - M) O_s /
 // sum_s 2^(m_s - M) l_s, lse = (M + log2(sum)) * ln 2.  128 threads x 4 dims.
+// blockIdx.y: the (layer, row) of the launch, or the tail unit.
 __global__ void __launch_bounds__(128) combine_kernel(const Params p) {
   // launched as a dependent of the attention kernel: its partials are
   // complete and visible once this returns
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int head = blockIdx.x;
-  const size_t rowL = blockIdx.y;
-  const int layer = static_cast<int>(rowL / p.rows);
-  const int row = static_cast<int>(rowL - (size_t)layer * p.rows);
-  const float *pm = p.part_ml + (rowL * p.nsplit * kH) * 2;
+  int layer, row, ns;
+  size_t tile0;  // the unit's first partial tile
+  if (p.tail_nsplit > 0) {
+    const int u = p.tail_base + static_cast<int>(blockIdx.y);
+    layer = u % p.n_layers;
+    row = u / p.n_layers;
+    ns = p.tail_nsplit;
+    tile0 = (size_t)blockIdx.y * ns;
+  } else {
+    const size_t rowL = blockIdx.y;
+    layer = static_cast<int>(rowL / p.rows);
+    row = static_cast<int>(rowL - (size_t)layer * p.rows);
+    ns = p.nsplit;
+    tile0 = rowL * ns;
+  }
+  const float *pm = p.part_ml + (tile0 * kH) * 2;
   float M = -INFINITY;
-  for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, pm[((size_t)s * kH + head) * 2]);
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, pm[((size_t)s * kH + head) * 2]);
   const float ref = M == -INFINITY ? 0.0f : M;
   float den = 0.0f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int d = threadIdx.x * 4;
-  for (int s = 0; s < p.nsplit; ++s) {
+  for (int s = 0; s < ns; ++s) {
     const float ms = pm[((size_t)s * kH + head) * 2], ls = pm[((size_t)s * kH + head) * 2 + 1];
     const float f = exp2f(ms - ref);
     den += f * ls;
-    const float4 v = *reinterpret_cast<const float4 *>(p.part_o + ((rowL * p.nsplit + s) * kH + head) * kDv + d);
+    const float4 v = *reinterpret_cast<const float4 *>(p.part_o + ((tile0 + s) * kH + head) * kDv + d);
     acc.x += f * v.x;
     acc.y += f * v.y;
     acc.z += f * v.z;

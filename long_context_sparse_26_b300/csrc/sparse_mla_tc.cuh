@@ -271,14 +271,36 @@ __global__ void __launch_bounds__(Roles<F8KV>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // this block's (layer, row) unit, its split and the windows per split;
+  // unit u is layer u % n_layers of row u / n_layers.  Units from tail_base
+  // on (the last, partial wave of a launch with one split per unit) take
+  // tail_nsplit splits.  `tile` indexes the block's fp32 partial.
   const int nl = p.n_layers;
-  const int layer = blockIdx.x % nl;
-  const int rest = blockIdx.x / nl;
-  const int split = rest % p.nsplit;
-  const int row = rest / p.nsplit;
+  int layer_, split_, row_, bps_, nsplit_;
+  size_t tile_;
+  if (p.tail_nsplit > 0 && static_cast<int>(blockIdx.x) >= p.tail_base) {
+    const int t = static_cast<int>(blockIdx.x) - p.tail_base, tu = t / p.tail_nsplit;
+    const int u = p.tail_base + tu;
+    split_ = t - tu * p.tail_nsplit;
+    layer_ = u % nl;
+    row_ = u / nl;
+    bps_ = p.tail_bps;
+    nsplit_ = p.tail_nsplit;
+    tile_ = (size_t)tu * p.tail_nsplit + split_;
+  } else {
+    layer_ = blockIdx.x % nl;
+    const int rest = blockIdx.x / nl;
+    split_ = rest % p.nsplit;
+    row_ = rest / p.nsplit;
+    bps_ = p.blocks_per_split;
+    nsplit_ = p.nsplit;
+    tile_ = ((size_t)layer_ * p.rows + row_) * p.nsplit + split_;
+  }
+  const int layer = layer_, split = split_, row = row_, unit_splits = nsplit_;
+  const size_t tile = tile_;
   const int b = row / p.Q;
-  const int slot0 = split * p.blocks_per_split * kKeys;
-  int nblk = p.blocks_per_split;
+  const int slot0 = split * bps_ * kKeys;
+  int nblk = bps_;
   {
     const int remaining = (p.K - slot0 + kKeys - 1) / kKeys;
     nblk = remaining < nblk ? remaining : nblk;
@@ -794,8 +816,7 @@ __global__ void __launch_bounds__(Roles<F8KV>::kThreads, 1)
     ok = sm->status[0][0] && sm->status[0][1] && sm->status[0][2] && sm->status[0][3];
     // After the last GEMM 2 every MMA into O^T is complete; on an abort it
     // may not be, so its tensor memory is not read.
-    const size_t rowL = (size_t)layer * p.rows + row;
-    const bool one = p.nsplit == 1;
+    const bool one = unit_splits == 1;
     if (owner) {
       if (one) {
         if (p.lse[layer] != nullptr) {
@@ -803,7 +824,7 @@ __global__ void __launch_bounds__(Roles<F8KV>::kThreads, 1)
           p.lse[layer][(size_t)row * kH + head] = (ok && l > 0.0f) ? (m_ref + log2f(l)) * ln2 : -INFINITY;
         }
       } else {
-        float *pm = p.part_ml + ((rowL * p.nsplit + split) * kH) * 2;
+        float *pm = p.part_ml + (tile * kH) * 2;
         pm[head * 2 + 0] = ok ? m_ref : -INFINITY;
         pm[head * 2 + 1] = ok ? l : 0.0f;
       }
@@ -821,13 +842,12 @@ __global__ void __launch_bounds__(Roles<F8KV>::kThreads, 1)
   __syncthreads();
   {
     const bool ok = sm->status[0][0] && sm->status[0][1] && sm->status[0][2] && sm->status[0][3];
-    const size_t rowL = (size_t)layer * p.rows + row;
-    const bool one = p.nsplit == 1;
+    const bool one = unit_splits == 1;
     if (ok && nblk > 0) {
       tc_fence_after();
       const float *inv_l = sm->xa[0];
       const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      float *po = one ? nullptr : p.part_o + ((rowL * p.nsplit + split) * kH) * kDv;
+      float *po = one ? nullptr : p.part_o + (tile * kH) * kDv;
       __nv_bfloat16 *bo = one ? p.out[layer] + (size_t)row * kH * kDv : nullptr;
 #pragma unroll 1
       for (int c = warp >> 2; c < kDv / 128; c += R::kThreads / 128) {
@@ -852,7 +872,7 @@ __global__ void __launch_bounds__(Roles<F8KV>::kThreads, 1)
       }
     } else {
       uint4 *dst = one ? reinterpret_cast<uint4 *>(p.out[layer] + (size_t)row * kH * kDv)
-                       : reinterpret_cast<uint4 *>(p.part_o + ((rowL * p.nsplit + split) * kH) * kDv);
+                       : reinterpret_cast<uint4 *>(p.part_o + (tile * kH) * kDv);
       const int n16 = one ? kH * kDv * 2 / 16 : kH * kDv * 4 / 16;
       for (int i = threadIdx.x; i < n16; i += R::kThreads) dst[i] = make_uint4(0u, 0u, 0u, 0u);
     }

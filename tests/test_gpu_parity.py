@@ -177,6 +177,38 @@ def test_sparse_attention(B, Q, T, k, pad):
     assert np.abs(lse.cpu().double().numpy() - LSE).max() < 1e-3
 
 
+def test_attention_last_wave_split():
+    """More (layer, row) units than SMs, with a partial last wave: the units of
+    that wave are split and merged by the combine while the others run whole.
+    Every row against the oracle, lse included (one layer), and every row of a
+    two-layer shared launch shaped the same way."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    units = (sms + 4) // 4 * 4 + (4 if (sms + 4) % 4 else 0)  # a full wave and a few more, a multiple of 4
+    T, k = 3000, 2048
+    cfg = dsa.default_config(topk=k)
+    # one layer: units = rows
+    B, Q = 2, units // 2
+    q, kv, idx = _attn_inputs(B, Q, T, k, seed=units, pad=0)
+    out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, Q, 64, dtype=torch.float32, device=DEV)
+    dsa.sparse_mla_attn(cfg, q, kv, idx, out, lse, dsa.alloc_workspace(cfg, B, Q, T, 1))
+    torch.cuda.synchronize()
+    O, LSE = oracle.sparse_mla_attn(f64(q), f64(kv), idx.cpu().numpy(), SCALE)
+    check_attention(f64(out), O)
+    assert np.abs(lse.cpu().double().numpy() - LSE).max() < 1e-3
+    # two layers over one index set: units = 2 x rows
+    B2, Q2 = 2, units // 4
+    _, _, idx2 = _attn_inputs(B2, Q2, T, k, seed=units + 1, pad=0)
+    q2 = [wl.mla_queries(B2, Q2, 62, layer, DEV) for layer in range(2)]
+    kv2 = [wl.latent_cache(B2, T, 62, layer, DEV) for layer in range(2)]
+    outs = [torch.empty(B2, Q2, 64, 512, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    dsa.sparse_mla_attn_shared(cfg, q2, kv2, idx2, outs, dsa.alloc_workspace(cfg, B2, Q2, T, 2))
+    torch.cuda.synchronize()
+    for layer in range(2):
+        O2, _ = oracle.sparse_mla_attn(f64(q2[layer]), f64(kv2[layer]), idx2.cpu().numpy(), SCALE)
+        check_attention(f64(outs[layer]), O2)
+
+
 def test_sparse_attention_shared_layers():
     """Three layers over one shared index set (with padding slots) in one
     launch, each against the oracle on its own cache."""
