@@ -224,8 +224,9 @@ TopkShape topk_shape(int rows, int T, int sms) {
     s.chunk = T;
     return s;
   }
+  // (chunk, row) blocks: at most one wave of the scan (four blocks per SM)
   const int target = 4 * sms;
-  int n = (target + rows - 1) / rows;
+  int n = target / rows;
   const int max_chunks = (T + 4095) / 4096;  // chunks of at least 4096 scores
   n = n < max_chunks ? n : max_chunks;
   n = n < dsa::topk::kThreads ? n : dsa::topk::kThreads;  // the select block prefix-sums one count per thread
@@ -241,9 +242,6 @@ struct AttnShape {
   // on (the last, partial wave) take tail_nsplit splits of tail_bps windows
   long long tail_base = 0;
   int tail_nsplit = 0, tail_bps = 0;
-  long long blocks(long long rowsL) const {
-    return tail_nsplit > 0 ? tail_base + (rowsL - tail_base) * tail_nsplit : rowsL * nsplit;
-  }
   // (layer, row) units whose splits leave fp32 partials, and splits each
   long long partial_units(long long rowsL) const { return tail_nsplit > 0 ? rowsL - tail_base : (nsplit > 1 ? rowsL : 0); }
   int partial_splits() const { return tail_nsplit > 0 ? tail_nsplit : nsplit; }
