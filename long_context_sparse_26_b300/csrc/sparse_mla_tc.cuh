@@ -44,16 +44,17 @@
 //              memory); GEMM 2 a third: one thread issues these small MMAs at
 //              about half the rate the tensor pipe takes them, two or three
 //              keep it fed;
-//   last 4     softmax, O^T rescale, epilogue; warp w owns TMEM lanes
+//   last 4     softmax and O^T rescale; warp w owns TMEM lanes
 //              32*(w%4)..+31: heads 16*(w%4)..+15 of S (an M = 64 result
 //              sits in lanes 0-15 of each 32-lane quarter; both half-warps
 //              read them, 32 columns each) and dims 128c + 32*(w%4)..+31 of
 //              O^T chunk c.
 // Tensor memory: O^T in columns 0-255 (chunk c at 64c); the two S partials in
 // two window buffers of kKeys columns each, from 256 and from 384.
-// The epilogue writes the block's result straight from tensor memory (lane =
-// dim, so each head's stores from a warp are 32 consecutive dims): bf16 and
-// normalised with one split, else the unnormalised fp32 partial plus
+// Every warp of the block writes the result, one 128-dim chunk of O^T for
+// its lane quarter, straight from tensor memory (lane = dim, so each head's
+// stores from a warp are 32 consecutive dims): bf16 and normalised when the
+// block's (layer, row) is one split, else the unnormalised fp32 partial plus
 // (reference max, sum) per head for the combine kernel.
 #pragma once
 
