@@ -50,6 +50,27 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
   lc.numAttrs = 1;
   return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
 }
+// The same, in thread-block clusters of cx consecutive blocks.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                     unsigned cx, Args &&...args) {
+  cudaLaunchConfig_t lc;
+  std::memset(&lc, 0, sizeof(lc));
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cx;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 2;
+  return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
+}
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct DeviceState {
@@ -425,8 +446,50 @@ dsa_status_t launch_topk(const Layout &L, uint8_t *ws, const float *scores, cons
 
 // Enqueues the tensor-core attention kernel (and the split combine) for
 // filled-in Params over B sequences; encodes each layer's tensor maps.
-dsa_status_t enqueue_attention(const dsa::attn::Params &p, int B, cudaStream_t stream) {
+// How many clusters of cx attention blocks the current device runs at once
+// (cached per device, row format and cluster size; 0 when it cannot).
+int attention_clusters(bool fp8, int cx) {
+  static int cache[kMaxDevices][2][9];
+  static bool init = false;
+  int dev = 0;
+  if (cx < 2 || cx > 8 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!init) {
+    for (auto &d : cache)
+      for (auto &f : d)
+        for (int &c : f) c = -1;
+    init = true;
+  }
+  int &c = cache[dev][fp8 ? 1 : 0][cx];
+  if (c < 0) {
+    cudaLaunchConfig_t lc;
+    std::memset(&lc, 0, sizeof(lc));
+    lc.gridDim = dim3(static_cast<unsigned>(cx) * 64);
+    lc.blockDim = dim3(fp8 ? dsa::mla::Roles<true>::kThreads : dsa::mla::Roles<false>::kThreads);
+    lc.dynamicSmemBytes = dsa::mla::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cx);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int n = 0;
+    const cudaError_t e =
+        fp8 ? cudaOccupancyMaxActiveClusters(&n, dsa::mla::sparse_mla_tc_kernel<true>, &lc)
+            : cudaOccupancyMaxActiveClusters(&n, dsa::mla::sparse_mla_tc_kernel<false>, &lc);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    c = n;
+  }
+  return c;
+}
+
+dsa_status_t enqueue_attention(const dsa::attn::Params &p_in, int B, cudaStream_t stream) {
   (void)B;
+  dsa::attn::Params p = p_in;
   dsa::mla::Maps maps;
   std::memset(&maps, 0, sizeof(maps));
   for (int l = 0; l < p.n_layers; ++l)
@@ -434,17 +497,31 @@ dsa_status_t enqueue_attention(const dsa::attn::Params &p, int B, cudaStream_t s
       return DSA_ERR_CUDA;
   const long long rowsL = static_cast<long long>(p.n_layers) * p.rows;
   const long long blocks = p.tail_nsplit > 0 ? p.tail_base + (rowsL - p.tail_base) * p.tail_nsplit : rowsL * p.nsplit;
+  // Several splits per unit, all units in one wave of clusters: each unit's
+  // splits form a cluster that merges them itself (no partials in global
+  // memory, no combine launch).
+  p.cluster = (p.tail_nsplit == 0 && (p.nsplit == 2 || p.nsplit == 4 || p.nsplit == 8) &&
+               attention_clusters(p.kv_fp8 != 0, p.nsplit) >= rowsL)
+                  ? 1
+                  : 0;
   // a programmatic dependent launch: the blocks may start (barriers, tensor
   // memory, the query panels) while the kernel before them on the stream
   // finishes; they wait for it (griddepcontrol.wait) before reading idx
   const dim3 grid(static_cast<unsigned>(blocks));
   const dim3 block(p.kv_fp8 ? dsa::mla::Roles<true>::kThreads : dsa::mla::Roles<false>::kThreads);
-  const cudaError_t e =
-      p.kv_fp8 ? launch_dependent(dsa::mla::sparse_mla_tc_kernel<true>, grid, block, dsa::mla::kSmemBytes, stream, maps, p)
-               : launch_dependent(dsa::mla::sparse_mla_tc_kernel<false>, grid, block, dsa::mla::kSmemBytes, stream, maps,
-                                  p);
+  cudaError_t e;
+  if (p.cluster)
+    e = p.kv_fp8 ? launch_dependent_cluster(dsa::mla::sparse_mla_tc_kernel<true>, grid, block, dsa::mla::kSmemBytes,
+                                            stream, static_cast<unsigned>(p.nsplit), maps, p)
+                 : launch_dependent_cluster(dsa::mla::sparse_mla_tc_kernel<false>, grid, block, dsa::mla::kSmemBytes,
+                                            stream, static_cast<unsigned>(p.nsplit), maps, p);
+  else
+    e = p.kv_fp8 ? launch_dependent(dsa::mla::sparse_mla_tc_kernel<true>, grid, block, dsa::mla::kSmemBytes, stream,
+                                    maps, p)
+                 : launch_dependent(dsa::mla::sparse_mla_tc_kernel<false>, grid, block, dsa::mla::kSmemBytes, stream,
+                                    maps, p);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
-  if (p.nsplit > 1 || p.tail_nsplit > 0) {
+  if (!p.cluster && (p.nsplit > 1 || p.tail_nsplit > 0)) {
     const long long cunits = p.tail_nsplit > 0 ? rowsL - p.tail_base : rowsL;
     const dim3 cgrid(kHeads, static_cast<unsigned>(cunits));
     if (launch_dependent(dsa::attn::combine_kernel, cgrid, dim3(128), 0, stream, p) != cudaSuccess)

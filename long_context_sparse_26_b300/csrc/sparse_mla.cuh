@@ -41,6 +41,10 @@ struct Params {
   // tail_nsplit splits of tail_bps windows instead (tail_nsplit 0: none;
   // then nsplit is 1); their partials are tiles (u - tail_base) * tail_nsplit + split
   int tail_base, tail_nsplit, tail_bps;
+  // 1: the nsplit splits of each unit are one thread-block cluster (blocks
+  // u * nsplit .. u * nsplit + nsplit - 1 for unit u), which merges them
+  // itself through distributed shared memory: no partials, no combine
+  int cluster;
   float *part_o;                        // [n_layers*rows, nsplit, 64, 512], or the tail units' tiles
   float *part_ml;                       // [n_layers*rows, nsplit, 64, 2], likewise
   float scale_log2;                     // sm_scale * log2(e)

@@ -105,7 +105,7 @@ constexpr int kTmemCols = 512;
 constexpr int kOCol = 0;
 constexpr int kSCol = 256;                           // S partial of groups 0, 2, 4; two window buffers
 constexpr int kSColB = 384;                          // S partial of groups 1, 3; two window buffers
-constexpr int kSmallBytes = 2048;
+constexpr int kSmallBytes = 4096;
 constexpr int kSmemBytes = 1024 + kQBytes + kRingBytes + kSmallBytes;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 static_assert(kRingBytes >= kH * kDv * 4, "the epilogue stages an fp32 partial in the gather ring");
@@ -145,6 +145,31 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // cp.async this thread issued before has landed.
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Thread-block clusters: a barrier over every thread of every CTA of the
+// cluster (arrive with release, wait with acquire), and loads from another
+// CTA's shared memory at the address a local one maps to.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -219,8 +244,13 @@ __device__ __forceinline__ int checked_pos(int raw, int T, bool report) {
   return raw;
 }
 
+constexpr int kMaxClusterSplits = 8;
+
 struct Small {
   alignas(16) float xa[2][kH];    // per-head rescale factors (1/l for the epilogue)
+  alignas(16) float cml[kH][2];   // cluster launch: this split's (reference max, sum) per head
+  alignas(16) float cw[kH][kMaxClusterSplits];  // cluster launch: each split's weight in the merge, per head
+  float cinv[kH];                 // cluster launch: 1 / the merged sum, per head
   uint64_t full[kWindows][kGroups];   // a group of a window slot has landed (producer arrivals)
   uint64_t empty[kWindows][kGroups];  // a group of a window slot is free (GEMM 2 commits)
   uint64_t s_full[2];
@@ -279,7 +309,16 @@ __global__ void __launch_bounds__(Roles<F8KV>::kThreads, 1)
   const int nl = p.n_layers;
   int layer_, split_, row_, bps_, nsplit_;
   size_t tile_;
-  if (p.tail_nsplit > 0 && static_cast<int>(blockIdx.x) >= p.tail_base) {
+  if (p.cluster) {
+    // the splits of a unit are consecutive blocks (one cluster); tile unused
+    split_ = blockIdx.x % p.nsplit;
+    const int u = blockIdx.x / p.nsplit;
+    layer_ = u % nl;
+    row_ = u / nl;
+    bps_ = p.blocks_per_split;
+    nsplit_ = p.nsplit;
+    tile_ = 0;
+  } else if (p.tail_nsplit > 0 && static_cast<int>(blockIdx.x) >= p.tail_base) {
     const int t = static_cast<int>(blockIdx.x) - p.tail_base, tu = t / p.tail_nsplit;
     const int u = p.tail_base + tu;
     split_ = t - tu * p.tail_nsplit;
@@ -818,7 +857,10 @@ __global__ void __launch_bounds__(Roles<F8KV>::kThreads, 1)
     // After the last GEMM 2 every MMA into O^T is complete; on an abort it
     // may not be, so its tensor memory is not read.
     const bool one = unit_splits == 1;
-    if (owner) {
+    if (owner && p.cluster) {
+      sm->cml[head][0] = ok ? m_ref : -INFINITY;
+      sm->cml[head][1] = ok ? l : 0.0f;
+    } else if (owner) {
       if (one) {
         if (p.lse[layer] != nullptr) {
           const float ln2 = 0.69314718055994531f;
@@ -848,7 +890,9 @@ __global__ void __launch_bounds__(Roles<F8KV>::kThreads, 1)
       tc_fence_after();
       const float *inv_l = sm->xa[0];
       const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      float *po = one ? nullptr : p.part_o + (tile * kH) * kDv;
+      // a cluster launch stages the partial in this block's idle ring
+      // (every copy and MMA into it has completed) for the merge below
+      float *po = one ? nullptr : (p.cluster ? reinterpret_cast<float *>(sK) : p.part_o + (tile * kH) * kDv);
       __nv_bfloat16 *bo = one ? p.out[layer] + (size_t)row * kH * kDv : nullptr;
 #pragma unroll 1
       for (int c = warp >> 2; c < kDv / 128; c += R::kThreads / 128) {
@@ -873,10 +917,67 @@ __global__ void __launch_bounds__(Roles<F8KV>::kThreads, 1)
       }
     } else {
       uint4 *dst = one ? reinterpret_cast<uint4 *>(p.out[layer] + (size_t)row * kH * kDv)
-                       : reinterpret_cast<uint4 *>(p.part_o + (tile * kH) * kDv);
+                       : (p.cluster ? reinterpret_cast<uint4 *>(sK)
+                                    : reinterpret_cast<uint4 *>(p.part_o + (tile * kH) * kDv));
       const int n16 = one ? kH * kDv * 2 / 16 : kH * kDv * 4 / 16;
       for (int i = threadIdx.x; i < n16; i += R::kThreads) dst[i] = make_uint4(0u, 0u, 0u, 0u);
     }
+  }
+
+  // ---- cluster launch: the unit's splits merge among themselves.  Every
+  // CTA's partial O (staged above as [head][dim] fp32 in its ring) and its
+  // (max, sum) per head are visible cluster-wide after the first barrier;
+  // CTA `split` then merges dims [split * D, split * D + D), D = 512 / nsplit,
+  // exactly as the combine kernel does, and the second barrier keeps every
+  // CTA's shared memory alive until the others have read it.
+  if (p.cluster) {
+    const int ns = p.nsplit;
+    cluster_sync_all();
+    if (threadIdx.x < kH) {
+      const int h = threadIdx.x;
+      const uint32_t ml_local = smem_u32(&sm->cml[h][0]);
+      float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < ns; ++s2) {
+        const float2 v = ld_cluster_f2(cluster_map(ml_local, s2));
+        ms[s2] = v.x;
+        ls[s2] = v.y;
+        M = fmaxf(M, v.x);
+      }
+      const float ref = M == -INFINITY ? 0.0f : M;
+      float den = 0.0f;
+      for (int s2 = 0; s2 < ns; ++s2) {
+        const float f = exp2f(ms[s2] - ref);
+        sm->cw[h][s2] = f;
+        den += f * ls[s2];
+      }
+      sm->cinv[h] = den > 0.0f ? 1.0f / den : 0.0f;
+      if (split == 0 && p.lse[layer] != nullptr)
+        p.lse[layer][(size_t)row * kH + h] = den > 0.0f ? (M + log2f(den)) * 0.69314718055994531f : -INFINITY;
+    }
+    __syncthreads();
+    const int D = kDv / ns, q4n = D / 4;
+    const uint32_t stage = smem_u32(sK);
+    __nv_bfloat16 *orow = p.out[layer] + (size_t)row * kH * kDv;
+    for (int it = threadIdx.x; it < kH * q4n; it += R::kThreads) {
+      const int h = it / q4n, d = split * D + (it - h * q4n) * 4;
+      const uint32_t off = stage + static_cast<uint32_t>((h * kDv + d) * 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s2 = 0; s2 < ns; ++s2) {
+        const float f = sm->cw[h][s2];
+        const float4 v = ld_cluster_f4(cluster_map(off, s2));
+        acc.x += f * v.x;
+        acc.y += f * v.y;
+        acc.z += f * v.z;
+        acc.w += f * v.w;
+      }
+      const float inv = sm->cinv[h];
+      uint2 packed;
+      packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2 *>(orow + (size_t)h * kDv + d) = packed;
+    }
+    cluster_sync_all();
   }
 
   tc_fence_before();

@@ -177,6 +177,24 @@ def test_sparse_attention(B, Q, T, k, pad):
     assert np.abs(lse.cpu().double().numpy() - LSE).max() < 1e-3
 
 
+@pytest.mark.parametrize("B", [16, 32, 64])
+def test_attention_split_units(B):
+    """Units with 8, 4 and 2 splits (16, 32, 64 rows of k = 2048 on 148 SMs):
+    where every unit's splits fit the GPU at once as one thread-block cluster,
+    the cluster merges them itself; every row against the oracle, lse
+    included."""
+    cfg = dsa.default_config()
+    Q, T, k = 1, 3000, 2048
+    q, kv, idx = _attn_inputs(B, Q, T, k, seed=B + 5, pad=3)
+    out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, Q, 64, dtype=torch.float32, device=DEV)
+    dsa.sparse_mla_attn(cfg, q, kv, idx, out, lse, dsa.alloc_workspace(cfg, B, Q, T, 1))
+    torch.cuda.synchronize()
+    O, LSE = oracle.sparse_mla_attn(f64(q), f64(kv), idx.cpu().numpy(), SCALE)
+    check_attention(f64(out), O)
+    assert np.abs(lse.cpu().double().numpy() - LSE).max() < 1e-3
+
+
 def test_attention_last_wave_split():
     """More (layer, row) units than SMs, with a partial last wave: the units of
     that wave are split and merged by the combine while the others run whole.
