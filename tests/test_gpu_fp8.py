@@ -122,6 +122,7 @@ def test_fp8kv_group_verify_small():
     (3, 1, 3000, 100, 0),        # ragged last block
     (1, 1, 40, 2048, 0),         # fewer rows than slots
     (40, 8, 2500, 256, 0),       # many rows: single split, no combine
+    (32, 1, 3000, 2048, 3),      # four splits a row: merged by a cluster where they fit the GPU at once
 ])
 def test_fp8_latent_attention(B, Q, T, k, pad):
     cfg = dsa.default_config(topk=k)
