@@ -245,8 +245,8 @@ TopkShape topk_shape(int rows, int T, int sms) {
     s.chunk = T;
     return s;
   }
-  // (chunk, row) blocks: at most one wave of the scan (four blocks per SM)
-  const int target = 4 * sms;
+  // (chunk, row) blocks: at most one wave of the scan (two blocks per SM)
+  const int target = 2 * sms;
   int n = target / rows;
   const int max_chunks = (T + 4095) / 4096;  // chunks of at least 4096 scores
   n = n < max_chunks ? n : max_chunks;

@@ -308,9 +308,9 @@ __device__ __forceinline__ RowPlan plan_row_global(const uint32_t *g, uint32_t K
 // counted but not written.  PASS 1 chooses digit 0 > b0 (>= b0 with
 // take_b0) and, given hist1, counts digit 1 of bin b0 into it; PASS 2 chooses
 // bin b0 at sub-bin b1 or above.  Returns the count (the same in every thread).
-// PREFETCH: the next iteration's scores are loaded before this iteration's
-// block-wide prefix sum (8 more registers a thread).
-template <int PASS, bool PREFETCH = true>
+// The next iteration's scores are loaded before this iteration's block-wide
+// prefix sum.
+template <int PASS>
 __device__ uint32_t scan_ordered(const float *srow, int start, int end, const RowPlan &rp, uint32_t b1,
                                  uint32_t *hist1, uint64_t *dst, uint32_t cap, Scratch *sc) {
   uint32_t count = 0;
@@ -340,17 +340,13 @@ __device__ uint32_t scan_ordered(const float *srow, int start, int end, const Ro
     }
   };
   float nxt[8];
-  if (PREFETCH && start < end) load8(start, nxt);
+  if (start < end) load8(start, nxt);
   for (int base = start; base < end; base += kThreads * 8) {  // block-uniform trip count
     const int i0 = base + threadIdx.x * 8;
     float val[8];
-    if constexpr (PREFETCH) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) val[u] = nxt[u];
-      if (base + kThreads * 8 < end) load8(base + kThreads * 8, nxt);
-    } else {
-      load8(base, val);
-    }
+    for (int u = 0; u < 8; ++u) val[u] = nxt[u];
+    if (base + kThreads * 8 < end) load8(base + kThreads * 8, nxt);
     uint32_t takes = 0;
     if (PASS == 1) {
 #pragma unroll
@@ -623,7 +619,7 @@ struct ChunkParams {
 
 constexpr int kGhistStride = kBins0;  // per-row words of ghist
 // The row's last block copies up to this many candidates into its dynamic
-// shared memory (40 KB: four 512-thread blocks of the scan still fit an SM)
+// shared memory (40 KB a block, two blocks of the scan an SM)
 // and selects there; a row with more reads them in place from L2.
 constexpr int kSelCap = 5120;
 constexpr int kScanSelectSmem = kSelCap * 8;
@@ -726,7 +722,10 @@ __device__ void select_from_chunks(const uint64_t *crow, int chunk, int nvalid, 
 // the chunk's slice, with their count.  The block that finishes its row last
 // (a ticket taken after the block's writes are fenced; no block waits on
 // another) selects the row's k winners from the slices.
-__global__ void __launch_bounds__(kThreads, 4) topk_chunk_scan_select_kernel(const ChunkParams p) {
+// Two 512-thread blocks an SM: 64 registers a thread leave room for the
+// scan's prefetch (measured at 1M: 39.1 -> 34.2 us for the standalone
+// select, against four blocks an SM without it).
+__global__ void __launch_bounds__(kThreads, 2) topk_chunk_scan_select_kernel(const ChunkParams p) {
   extern __shared__ __align__(16) uint64_t s_cand[];  // kSelCap
   __shared__ uint32_t hist[kBins];
   __shared__ uint32_t ccnt[kThreads];
@@ -750,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 4) topk_chunk_scan_select_kernel(con
   rp.take_b0 = true;
   const uint64_t *crow = p.cand + (size_t)row * p.T;
   // never exceeded: positions are distinct
-  const uint32_t n = scan_ordered<1, false>(p.scores + (size_t)row * p.T, start, end, rp, 0, nullptr,
+  const uint32_t n = scan_ordered<1>(p.scores + (size_t)row * p.T, start, end, rp, 0, nullptr,
                                      p.cand + (size_t)row * p.T + start, static_cast<uint32_t>(end - start), &sc);
   if (threadIdx.x == 0) p.counts[(size_t)row * p.nchunk + c] = n;
   // the kernel after this one (the attention, a dependent launch) may start
