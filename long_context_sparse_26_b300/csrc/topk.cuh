@@ -773,20 +773,20 @@ __global__ void __launch_bounds__(kThreads, 2) topk_chunk_scan_select_kernel(con
     select_from_chunks(crow, p.chunk, nvalid, ccnt, rp, p.K, hist, qoff, out, &sc);
     return;
   }
-  // the chunks, in order, into shared memory (one pass over L2, every load
-  // independent: entry i of the gathered list belongs to the last chunk whose
-  // offset is <= i), then every radix pass and the ordered write in shared memory
-  for (uint32_t i = threadIdx.x; i < ncand; i += kThreads) {
-    int lo = 0, hi = nvalid;  // first chunk with offset > i is hi
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (qoff[mid] <= i) lo = mid + 1; else hi = mid;
+  // the chunks, in order, into shared memory (one pass over L2: warp w
+  // copies chunks w, w + 16, ... to their offsets with asynchronous 8-byte
+  // copies, none waiting for another; measured 1.8 us faster at 1M than a
+  // search for each entry's chunk), then every radix pass and the ordered
+  // write in shared memory
+  {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int cc = warp; cc < nvalid; cc += kThreads / 32) {
+      const uint64_t *src = crow + (size_t)cc * p.chunk;
+      const uint32_t m = ccnt[cc];
+      uint64_t *dst = s_cand + qoff[cc];
+      for (uint32_t i = lane; i < m; i += 32)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst + i)), "l"(src + i) : "memory");
     }
-    const int cc = lo - 1;
-    // an asynchronous 8-byte copy: no load waits for another
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(s_cand + i)),
-                 "l"(crow + (size_t)cc * p.chunk + (i - qoff[cc]))
-                 : "memory");
   }
   cp_async_commit();
   cp_async_wait<0>();
