@@ -337,8 +337,8 @@ def test_group_tiny_decode():
 
 
 def test_group_equals_four_independent_layers():
-    """North-star check (b) on the GPU: the group call equals four single-layer
-    calls fed the group's index set, bit for bit."""
+    """IndexShare on the GPU: the group call equals four single-layer calls fed
+    the group's index set, bit for bit."""
     w_ = wl.TINY
     cfg = dsa.default_config()
     inp = wl.make_inputs(w_, DEV)

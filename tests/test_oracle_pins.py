@@ -227,7 +227,7 @@ def _tiny_group_inputs(rng, B=2, Q=2, H_I=3, D_I=6, H=2, Dqk=10, T=24, n_layers=
 
 
 def pin_group_reuses_one_index_set(o):
-    """North-star check (b): a group equals 4 independent sparse layers on the same indices."""
+    """IndexShare: a group equals 4 independent sparse layers on the same indices."""
     rng = np.random.default_rng(8)
     q_idx, w, k_idx, q_pos, qs, kvs = _tiny_group_inputs(rng)
     k, scale, Dv = 5, 0.3, 6
@@ -293,7 +293,7 @@ def pin_mtp_reuse_and_kv_share(o):
 
 
 def pin_indexer_flops(o):
-    """North-star check (d): sharing one indexer over 4 layers divides its work by exactly 4."""
+    """IndexShare: sharing one indexer over 4 layers divides its work by exactly 4."""
     T = 1 << 20
     shared = o.indexer_flops(T, 4, True)
     per_layer = o.indexer_flops(T, 4, False)
