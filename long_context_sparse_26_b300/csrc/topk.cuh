@@ -43,8 +43,9 @@
 //     from the complete histogram and write every score of bin b0 or above,
 //     in position order, into their own chunk's slice of a per-row buffer
 //     with a count, and the block that finishes its row last (an atomic
-//     ticket; no block ever waits on another) does step 4 reading the
-//     slices in place.  Bin b0 is always taken whole there, so these rows
+//     ticket; no block ever waits on another) does step 4 on the slices,
+//     copied into its shared memory (or read in place in L2 when they hold
+//     more than it does).  Bin b0 is always taken whole there, so these rows
 //     need no second digit and no cap on the candidate count.
 // In the one-block-per-row shape, if a row has more candidates than the
 // select buffer holds (thousands of exactly equal scores), three exact radix
